@@ -1,0 +1,446 @@
+"""Benchmark of one paged-attention decode step on GB300.
+
+A step is the whole hot path for one batch: reshape_and_cache of every sequence's new
+K/V row, then the paged decode (pa_decode_step = reshape + pa_decode_auto), on the
+Llama-3-8B-shaped GQA workload (256 sequences, 32 query / 8 kv heads, head size 128,
+block size 16, bf16, lognormal contexts).  Prints ONE JSON line.
+
+  value    device-resident throughput: algorithmic bytes (K+V of every context token
+           and kv head, plus Q and out) per second, inputs already in HBM;
+  e2e      the same metric through the public API with the step's inputs copied from
+           pinned host memory (host allocator append, H2D of q/k/v/metadata, the step,
+           D2H of out, synchronise) -- every step;
+  roofline the decode kernel alone (CUDA events recorded by the library around that
+           launch) against the measured HBM copy bandwidth.
+
+--impl reference times the fp64 CPU oracle (the baseline arm) on a bounded sample of
+the same workload.  Under torchrun every rank runs its own replica (weak scaling);
+rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn effective KV HBM GB/s (% of GB300 peak); seq-tokens/s per layer"
+WORKLOAD = "l3_8b"
+SPEC_HBM_GBS = 8000.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_187_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record():
+    """dram bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel sources (same hash); else None."""
+    path = os.path.join(ROOT, "profiles", "paged_decode_l3_8b_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources_sha256_16") != _kernel_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t_start and self.t_start <= r[0] <= (self.t_stop or 1e30)]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unparsed nvidia-smi output"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole run (timed region shorter than the sampling period)"}
+
+
+def _smi_index(cuda_index: int) -> str:
+    """nvidia-smi's id of the CUDA device (CUDA_VISIBLE_DEVICES renumbers devices)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if cuda_index < len(ids):
+            return ids[cuda_index]
+    return str(cuda_index)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def time_oracle(r, budget_s: float = 15.0):
+    """Times the fp64 oracle (single thread) on whole sequences of the runner's current
+    step, in batch order, until about `budget_s` of CPU work has been spent."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from oracle_side import OracleState, record_step
+    st = record_step(r)
+    w = r.w
+    chosen, spent, nbytes, ntok = [], 0.0, 0, 0
+    # estimate per-token cost on a short prefix first
+    for s in range(w.num_seqs):
+        chosen.append(s)
+        o = OracleState(r, [st], seqs=[s])
+        only = np.zeros((w.num_seqs, w.num_q_heads), np.uint8)
+        only[s, :] = 1
+        t0 = time.perf_counter()
+        oracle.decode_v1(st.q, o.k_cache, o.v_cache, o.tables(0), o.step_lens[0],
+                         np.float32(w.scale), w.dtype, only=only)
+        spent += time.perf_counter() - t0
+        L = int(r.context_lens[s])
+        nbytes += L * w.num_kv_heads * w.head_size * 2 * 2 + 2 * w.num_q_heads * w.head_size * 2
+        ntok += L
+        if spent >= budget_s:
+            break
+    return {"seconds": spent, "bytes": nbytes, "tokens": ntok, "seqs": len(chosen)}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import torch
+    from paged_kv_cache_187_gb300 import workloads as W
+    from paged_kv_cache_187_gb300.runner import DecodeRunner
+    w = W.WORKLOADS[WORKLOAD]
+    r = DecodeRunner(w, device="cuda").next_step()
+    r.run_reshape()
+    torch.cuda.synchronize()
+    per_step_budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(r, per_step_budget)
+    samples = [time_oracle(r, per_step_budget) for _ in range(args.steps)]
+    sec = sum(x["seconds"] for x in samples)
+    byt = sum(x["bytes"] for x in samples)
+    tok = sum(x["tokens"] for x in samples)
+    gbs = byt / sec / 1e9
+    sample = (f"each step: the fp64 oracle (one thread) over whole sequences of the {w.name} "
+              f"batch in order until ~{per_step_budget:.1f} s; {samples[0]['seqs']} seqs, "
+              f"{samples[0]['tokens']} context tokens in step 1")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w, r),
+        "seq_tokens_per_s": tok / sec,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, r):
+    return {
+        "workload": f"{w.name}: {w.description}: {w.num_seqs} seqs, {w.num_q_heads} q / "
+                    f"{w.num_kv_heads} kv heads, head_size {w.head_size}, block_size "
+                    f"{w.block_size}, {w.dtype}, contexts lognormal(6.9, 0.8) clipped [16, 8192]",
+        "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+        "head_size": w.head_size, "block_size": w.block_size,
+        "context_tokens": int(r.context_lens.sum()), "max_context_len": int(r.context_lens.max()),
+        "step": "pa_decode_step: reshape_and_cache of the new tokens + pa_decode_auto",
+        "l2": f"no flush: {r.kv_bytes() / 1e9:.2f} GB of K/V per step read once vs 129 MB L2",
+        "seed": w.seed,
+    }
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    import paged_kv_cache_187_gb300 as pa
+    from paged_kv_cache_187_gb300 import workloads as W
+    from paged_kv_cache_187_gb300.runner import DecodeRunner
+
+    w = W.WORKLOADS[WORKLOAD]
+    r = DecodeRunner(w, device=device, rank=rank).next_step()
+    stream = torch.cuda.current_stream(device)
+    variant, psize = pa.pa_decode_auto_plan(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                            w.head_size, w.block_size, r.step_max_context_len())
+    launches_per_step = 1 + (1 if variant == 1 else 2 + (1 if r.step_max_context_len() > psize else 0))
+    bytes_step = r.kv_bytes()
+    tokens_step = r.seq_tokens()
+
+    # ---- device-resident timing: K steps of reshape + decode
+    for _ in range(args.warmup):
+        r.run_step()
+    K = args.steps
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    for a, b in ev_k:            # materialise the CUDA events before handing them over
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(_smi_index(device.index or 0))
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize(device)
+    clocks.t_start = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        pa.pa_set_kernel_events(ev_k[i][0], ev_k[i][1])
+        r.run_step()
+    t_stop.record(stream)
+    torch.cuda.synchronize(device)
+    clocks.t_stop = time.time()
+    _barrier(ws)
+    pa.pa_set_kernel_events(None, None)
+    time.sleep(0.15)
+    clocks.stop()
+    ms_total = t_start.elapsed_time(t_stop)
+    ms_total = _max_over_ranks(ms_total, ws, device)
+    ms_step = ms_total / K
+    kern_ms = [a.elapsed_time(b) for a, b in ev_k]
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    torch.cuda.synchronize(device)
+    assert int(r.status.item()) == 0, f"device status {int(r.status.item())}"
+
+    value = ws * bytes_step / (ms_step * 1e-3) / 1e9
+    seq_tok_s = ws * tokens_step / (ms_step * 1e-3)
+
+    # ---- end-to-end through the public API from pinned host memory
+    e2e = run_e2e(args, w, device, rank, pa, W, DecodeRunner)
+    e2e_val = _max_over_ranks(-e2e["value"], ws, device)   # slowest rank
+    e2e["value"] = -e2e_val * ws
+
+    peak, peak_kind = _peaks()
+    achieved = bytes_step / (kern_avg_ms * 1e-3) / 1e9
+    traffic = _traffic_record()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": _config(w, r),
+        "seq_tokens_per_s": seq_tok_s,
+        "pct_of_spec_8000_GBps": 100.0 * value / ws / SPEC_HBM_GBS,
+        f"pct_of_{peak_kind}_hbm": 100.0 * value / ws / peak,
+        "decode_variant": {"variant": f"v{variant}", "partition_size": psize},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "paged_decode_kernel (persistent V2 decode; events around its launch)",
+                     "bytes_per_launch": bytes_step, "kernel_ms": kern_avg_ms,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        cb = time_oracle(r, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": cb["bytes"] / cb["seconds"] / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"fp64 oracle, one thread, first {cb['seqs']} sequences of one {w.name} "
+                      f"step ({cb['tokens']} context tokens, {cb['seconds']:.1f} s)",
+            "seq_tokens_per_s": cb["tokens"] / cb["seconds"],
+            "host_cpu_count": os.cpu_count(),
+        }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
+    """Synchronous serving loop through the public API: host allocator append, H2D of
+    the step's q/k/v and metadata from pinned memory, pa_decode_step, D2H of out."""
+    import dataclasses
+    import torch
+    K = min(args.steps, args.e2e_steps)
+    warm = 3
+    we = dataclasses.replace(w, steps=K + warm + 1)
+    r = DecodeRunner(we, device=device, rank=rank)
+    S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
+    tdt = W.torch_dtype(w)
+    ring = 4
+    qh = [W.randn_16bit((S, Hq, D), w.dtype, 900 + i, "cpu").pin_memory() for i in range(ring)]
+    kh = [W.randn_16bit((S, Hkv, D), w.dtype, 910 + i, "cpu").pin_memory() for i in range(ring)]
+    vh = [W.randn_16bit((S, Hkv, D), w.dtype, 920 + i, "cpu").pin_memory() for i in range(ring)]
+    meta_h = torch.empty(S * (2 + r.max_blocks), dtype=torch.int32).pin_memory()
+    out_h = torch.empty((S, Hq, D), dtype=tdt).pin_memory()
+    q_d = torch.empty((S, Hq, D), dtype=tdt, device=device)
+    k_d = torch.empty((S, Hkv, D), dtype=tdt, device=device)
+    v_d = torch.empty_like(k_d)
+    meta_d = torch.empty_like(meta_h, device=device)
+    meta_np = meta_h.numpy()
+    ids = r.seq_ids
+    stream = torch.cuda.current_stream(device)
+    total_bytes = 0
+    total_tok = 0
+    h2d = d2h = 0
+
+    def one(i, count):
+        nonlocal total_bytes, total_tok, h2d, d2h
+        slots = r.alloc.pa_alloc_append_batch(ids)
+        tables = r.alloc.pa_alloc_block_tables(ids, r.max_blocks)
+        lens = r.alloc.pa_alloc_context_lens(ids)
+        meta_np[:S] = slots
+        meta_np[S:2 * S] = lens
+        meta_np[2 * S:] = tables.reshape(-1)
+        q_d.copy_(qh[i % ring], non_blocking=True)
+        k_d.copy_(kh[i % ring], non_blocking=True)
+        v_d.copy_(vh[i % ring], non_blocking=True)
+        meta_d.copy_(meta_h, non_blocking=True)
+        pa.pa_decode_step(r.out, q_d, k_d, v_d, r.key_cache, r.value_cache, meta_d[:S],
+                          meta_d[2 * S:].view(S, r.max_blocks), meta_d[S:2 * S],
+                          int(lens.max()), w.scale, workspace=r.workspace, status=r.status,
+                          stream=stream)
+        out_h.copy_(r.out, non_blocking=True)
+        stream.synchronize()
+        if count:
+            L = lens.astype(np.int64)
+            total_bytes += int(L.sum()) * Hkv * D * 2 * 2 + 2 * S * Hq * D * 2
+            total_tok += int(L.sum())
+            h2d = (q_d.numel() + k_d.numel() + v_d.numel()) * 2 + meta_h.numel() * 4
+            d2h = out_h.numel() * 2
+
+    # the workspace must cover the longest context the loop will reach
+    need = pa.pa_decode_auto_workspace_size(S, Hq, Hkv, D, w.block_size, r.max_context_len + K + warm)
+    if need > r.workspace.numel():
+        r.workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    for i in range(warm):
+        one(i, False)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for i in range(K):
+        one(i, True)
+    dt = time.perf_counter() - t0
+    assert int(r.status.item()) == 0
+    return {"value": total_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": 1e3 * dt / K,
+            "seq_tokens_per_s": total_tok / dt,
+            "path": "pa_alloc_append_batch + block tables on the host, pinned H2D, "
+                    "pa_decode_step, D2H of out, stream sync; wall clock"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

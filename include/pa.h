@@ -1,0 +1,227 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-attention decode library (libpa.so).
+ *
+ * What the library computes comes from three web pages, cited by title and part:
+ *   [TALK] "vLLM Project Update" (Bay.Area.AI talk transcript): PagedAttention is an
+ *          attention algorithm over blocks of KV cache managed like virtual-memory
+ *          pages; the first kernel gave each sequence to one SM, which left SMs
+ *          unevenly loaded; the V2 kernel partitions each sequence into pieces spread
+ *          over SMs, "similar to flash decoding".
+ *   [HN]   "vLLM: Easy, Fast, and Cheap LLM Serving with PagedAttention" (Hacker News
+ *          thread): PagedAttention still computes exact attention; the KV cache of one
+ *          LLaMA-13B sequence is up to 1.7 GB.
+ *   [PR]   "[core] Multi Step Scheduling #7000": the decode metadata slot_mapping,
+ *          block_tables and seq_lens, advanced between the steps of a multi-step
+ *          decode loop, and the v2 block manager that hands out physical blocks.
+ *
+ * Conventions shared by every call
+ *   Ownership.  The caller owns every buffer.  Device buffers are plain device
+ *     pointers (for example from torch); the library never allocates, frees or
+ *     retains them.  The decode calls that need scratch take a caller-provided device
+ *     workspace sized by the matching *_workspace_size call.
+ *   Layouts.  All tensors are dense and row-major, in elements of the call's dtype:
+ *       query, out          [num_seqs][num_q_heads][head_size]
+ *       key, value (new)    [num_tokens][num_kv_heads][head_size]
+ *       key_cache,
+ *       value_cache         [num_blocks][num_kv_heads][block_size][head_size]
+ *       block_tables        int32 [num_seqs][max_blocks_per_seq]; entry j of row s is
+ *                           the physical block holding tokens j*block_size ..
+ *                           (j+1)*block_size-1 of sequence s; entries past the
+ *                           sequence's last block are never read (pad with -1).
+ *       context_lens        int32 [num_seqs], tokens of each sequence INCLUDING the
+ *                           token of this step, which reshape_and_cache wrote first.
+ *       slot_mapping        int32 [num_tokens], flat slot block*block_size+offset per
+ *                           new token; a negative slot marks a padding token.
+ *     Query head h attends through kv head h / (num_q_heads / num_kv_heads).
+ *     Device pointers must be 16-byte aligned.
+ *   Supported shapes.  head_size 64 or 128; block_size 16 or 32; num_q_heads a
+ *     multiple of num_kv_heads with a group of at most 16; fp16 or bf16.  Other
+ *     combinations return PA_ERR_UNSUPPORTED.
+ *   Streams.  Every device call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and never synchronises the host.
+ *   Errors.  Calls return a pa_status; pa_last_error() gives this thread's message
+ *     for the last failure.  Host-detectable errors (bad sizes, null pointers) are
+ *     reported before any launch.  Errors only the device can see (a slot or block-
+ *     table entry outside the pool, a context longer than max_context_len or than
+ *     the block-table row, a pipeline wait that exceeded its time limit) never fault:
+ *     the offending access is skipped, and if `status_dev` is not NULL the kernel ORs
+ *     the matching PA_DEVERR_* bit into that device int32.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent sizes */
+    PA_ERR_UNSUPPORTED = 2,   /* dtype / head_size / block_size / group not built */
+    PA_ERR_NO_BLOCKS = 3,     /* allocator: not enough free blocks (nothing changed) */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
+    PA_ERR_WORKSPACE = 5      /* workspace NULL or smaller than *_workspace_size */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Same type as cudaStream_t, so callers without CUDA headers can still link. */
+typedef struct CUstream_st* pa_stream;
+
+/* Bits a kernel ORs into *status_dev. */
+#define PA_DEVERR_BAD_SLOT 1   /* slot_mapping entry >= num_blocks * block_size */
+#define PA_DEVERR_BAD_BLOCK 2  /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_BAD_LEN 4    /* context_len > max_context_len or > row capacity; clamped */
+#define PA_DEVERR_TIMEOUT 8    /* a shared-memory pipeline wait passed its time limit */
+
+/* Message of this thread's last failed call ("" if none).  Valid until the next call. */
+const char* pa_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t pa_version(void);
+
+/* ------------------------------------------------------------------------------ */
+/* reshape_and_cache                                                              */
+/* ------------------------------------------------------------------------------ */
+/* Scatters the K and V rows of each new token into the paged pools [PR, slot_mapping]:
+ *   key_cache[slot / block_size][h][slot % block_size][:] = key[i][h][:]
+ * and the same for value, for every token i with slot = slot_mapping[i] >= 0 and every
+ * kv head h.  A pure copy: bit-exact.  Slots beyond the pool are skipped and flagged
+ * PA_DEVERR_BAD_SLOT.  Two tokens with the same slot in one call race (undefined). */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                               void* value_cache, const int32_t* slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads, int32_t head_size,
+                               int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                               int32_t* status_dev, pa_stream stream);
+
+/* ------------------------------------------------------------------------------ */
+/* Paged decode attention                                                          */
+/* ------------------------------------------------------------------------------ */
+/* One new query token per sequence attends over its whole context [TALK, HN]:
+ *   out[s][h][:] = sum_t softmax_t(scale * q[s][h] . k_t) v_t,   t < context_lens[s],
+ * with k_t, v_t row t % block_size of physical block block_tables[s][t / block_size]
+ * for kv head h / group.  fp32 accumulation; the output is rounded to `dtype`.
+ * A context length of 0 gives a zero row.  max_context_len is an upper bound the
+ * host knows (no device read-back); longer contexts are clamped and flagged.
+ *
+ * pa_decode_v1: one work unit per (sequence, kv head) over the whole context -- the
+ *   first kernel of [TALK].  Needs no workspace. */
+pa_status pa_decode_v1(void* out, const void* query, const void* key_cache,
+                       const void* value_cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_size, int32_t block_size, int32_t num_blocks,
+                       int32_t max_context_len, float scale, pa_dtype dtype,
+                       int32_t* status_dev, pa_stream stream);
+
+/* Bytes of device workspace pa_decode_v2 needs for these sizes. */
+size_t pa_decode_v2_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                   int32_t max_context_len, int32_t partition_size);
+
+/* pa_decode_v2: the V2 kernel of [TALK].  Each context is cut into partitions of
+ * partition_size tokens (a positive multiple of block_size); each (sequence, kv head,
+ * partition) is one work unit, handed to persistent CTAs from a shared counter.  A
+ * partition keeps its running max m_p and exp-sum l_p; sequences with more than one
+ * partition are merged by log-sum-exp, out = sum_p e^(m_p-M) acc_p / sum_p e^(m_p-M) l_p.
+ * `workspace` (device, 256-byte aligned, >= pa_decode_v2_workspace_size bytes) holds the
+ * work counter, the partition list and the partial results; its contents need no
+ * initialisation and are dead after the call. */
+pa_status pa_decode_v2(void* out, const void* query, const void* key_cache,
+                       const void* value_cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_size, int32_t block_size, int32_t num_blocks,
+                       int32_t max_context_len, float scale, pa_dtype dtype,
+                       int32_t partition_size, void* workspace, size_t workspace_bytes,
+                       int32_t* status_dev, pa_stream stream);
+
+/* Which variant pa_decode_auto runs for these host-known sizes.
+ * *variant = 1 (V1) or 2 (V2); *partition_size = the V2 partition size (0 for V1).
+ * The choice follows [TALK]: whole sequences per unit while there are enough units to
+ * fill every SM several times over and no context is long; partitions otherwise. */
+pa_status pa_decode_auto_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, int32_t block_size, int32_t max_context_len,
+                              int32_t* variant, int32_t* partition_size);
+
+/* Workspace bytes pa_decode_auto needs (0 when it picks V1). */
+size_t pa_decode_auto_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int32_t max_context_len);
+
+/* pa_decode_auto: runs pa_decode_v1 or pa_decode_v2 as pa_decode_auto_plan says. */
+pa_status pa_decode_auto(void* out, const void* query, const void* key_cache,
+                         const void* value_cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_size, int32_t block_size, int32_t num_blocks,
+                         int32_t max_context_len, float scale, pa_dtype dtype,
+                         void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                         pa_stream stream);
+
+/* One decode step of the hot path on device buffers: pa_reshape_and_cache of the
+ * step's new K/V rows, then pa_decode_auto, on the same stream. */
+pa_status pa_decode_step(void* out, const void* query, const void* key, const void* value,
+                         void* key_cache, void* value_cache, const int32_t* slot_mapping,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                         int32_t num_blocks, int32_t max_context_len, float scale,
+                         pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, pa_stream stream);
+
+/* Compute path for grouped-query attention (group >= 2): 1 (default) contracts the
+ * group's query heads with each K/V tile on the tensor cores (mma.sync m16n8k16, fp32
+ * accumulate); 0 uses the CUDA-core path that multi-head attention always takes.
+ * Process-wide; both paths meet the same tolerance. */
+pa_status pa_set_gqa_tensor_cores(int32_t enable);
+
+/* Profiling hook: when both are non-NULL (cudaEvent_t handles), every later decode
+ * call records `start_event` on its stream right before it launches the paged decode
+ * kernel and `stop_event` right after, so that the kernel alone can be timed with
+ * cudaEventElapsedTime.  NULL, NULL turns the hook off (the default).  Process-wide. */
+pa_status pa_set_kernel_events(void* start_event, void* stop_event);
+
+/* ------------------------------------------------------------------------------ */
+/* Host block allocator (the v2 block manager of [PR]; blocks as pages per [TALK])  */
+/* ------------------------------------------------------------------------------ */
+/* Host memory only; one handle must not be used from two threads at once.
+ * Spec: physical ids 0..num_blocks-1 are shuffled by Fisher-Yates (i from
+ * num_blocks-1 down to 1, j = r % (i+1), r the next splitmix64 output seeded with
+ * `seed`); the result is the free list, popped from its end.  add_seq pops
+ * ceil(num_tokens / block_size) blocks in logical order; append pops one block when
+ * the length is a multiple of block_size, then returns the slot of the new last
+ * position; free_seq pushes the blocks back in logical order.  A request that needs
+ * more blocks than are free returns PA_ERR_NO_BLOCKS and changes nothing. */
+typedef struct pa_alloc pa_alloc;
+
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed,
+                          pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* alloc);
+int32_t pa_alloc_num_free(const pa_alloc* alloc);
+/* Registers sequence seq_id (>= 0, not live) holding num_tokens tokens. */
+pa_status pa_alloc_add_seq(pa_alloc* alloc, int32_t seq_id, int32_t num_tokens);
+/* Appends one token to seq_id; *slot_out = its slot. */
+pa_status pa_alloc_append(pa_alloc* alloc, int32_t seq_id, int32_t* slot_out);
+/* Appends one token to each of n sequences (all or nothing); slots_out[i] = slot. */
+pa_status pa_alloc_append_batch(pa_alloc* alloc, const int32_t* seq_ids, int32_t n,
+                                int32_t* slots_out);
+/* Returns seq_id's blocks to the free list and forgets the sequence. */
+pa_status pa_alloc_free_seq(pa_alloc* alloc, int32_t seq_id);
+/* Slots of positions [start, start + n) of seq_id. */
+pa_status pa_alloc_slots(const pa_alloc* alloc, int32_t seq_id, int32_t start, int32_t n,
+                         int32_t* out);
+/* Block-table rows [n][max_blocks_per_seq] of the listed sequences, padded with -1. */
+pa_status pa_alloc_block_tables(const pa_alloc* alloc, const int32_t* seq_ids, int32_t n,
+                                int32_t max_blocks_per_seq, int32_t* out);
+/* Current lengths of the listed sequences. */
+pa_status pa_alloc_context_lens(const pa_alloc* alloc, const int32_t* seq_ids, int32_t n,
+                                int32_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

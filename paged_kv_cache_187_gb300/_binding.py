@@ -1,0 +1,342 @@
+"""ctypes binding of libpa.so: the C ABI of include/pa.h with the same names.
+
+Argument marshalling only.  Every function takes torch tensors (for device buffers)
+or numpy arrays (for the host allocator), checks dtype / shape / device / contiguity,
+derives the sizes the C call needs, and passes raw pointers.  All arithmetic happens
+in the CUDA library; there is no fallback.  Importing this module on a machine
+without the built library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_NO_BLOCKS = 3
+PA_ERR_CUDA = 4
+PA_ERR_WORKSPACE = 5
+
+PA_F16 = 0
+PA_BF16 = 1
+
+PA_DEVERR_BAD_SLOT = 1
+PA_DEVERR_BAD_BLOCK = 2
+PA_DEVERR_BAD_LEN = 4
+PA_DEVERR_TIMEOUT = 8
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"pa status {status}: {message}")
+        self.status = status
+
+
+class PANoBlocks(PAError):
+    pass
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with paged_kv_cache_187_gb300.build.build() "
+            "(nvcc for sm_103a); this package has no CPU fallback")
+    lib = ctypes.CDLL(path)
+    P, i32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_float,
+                            ctypes.c_size_t)
+    sig = {
+        "pa_last_error": ([], ctypes.c_char_p),
+        "pa_version": ([], i32),
+        "pa_set_gqa_tensor_cores": ([i32], i32),
+        "pa_set_kernel_events": ([P, P], i32),
+        "pa_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
+        "pa_decode_v1": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P],
+                         i32),
+        "pa_decode_v2_workspace_size": ([i32, i32, i32, i32, i32], sz),
+        "pa_decode_v2": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32,
+                          P, sz, P, P], i32),
+        "pa_decode_auto_plan": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
+                                 ctypes.POINTER(i32)], i32),
+        "pa_decode_auto_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+        "pa_decode_auto": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P,
+                            sz, P, P], i32),
+        "pa_decode_step": ([P, P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                            i32, P, sz, P, P], i32),
+        "pa_alloc_create": ([i32, i32, u64, ctypes.POINTER(P)], i32),
+        "pa_alloc_destroy": ([P], None),
+        "pa_alloc_num_free": ([P], i32),
+        "pa_alloc_add_seq": ([P, i32, i32], i32),
+        "pa_alloc_append": ([P, i32, ctypes.POINTER(i32)], i32),
+        "pa_alloc_append_batch": ([P, P, i32, P], i32),
+        "pa_alloc_free_seq": ([P, i32], i32),
+        "pa_alloc_slots": ([P, i32, i32, i32, P], i32),
+        "pa_alloc_block_tables": ([P, P, i32, i32, P], i32),
+        "pa_alloc_context_lens": ([P, P, i32, P], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int):
+    if status != PA_OK:
+        msg = (_lib.pa_last_error() or b"").decode()
+        if status == PA_ERR_NO_BLOCKS:
+            raise PANoBlocks(status, msg)
+        raise PAError(status, msg)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def raw():
+    """The ctypes handle of libpa.so (all C symbols)."""
+    return _lib
+
+
+# --------------------------------------------------------------------------- helpers
+def _dt(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float16 or bfloat16)")
+
+
+def _dev(t, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _opt_dev(t, name):
+    import torch
+    if t is None:
+        return None
+    return _dev(t, name, torch.int32)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+# --------------------------------------------------------------------------- kernels
+def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None,
+                         stream=None):
+    """key/value [T, Hkv, D]; key_cache/value_cache [NB, Hkv, bs, D]; slot_mapping [T] int32."""
+    import torch
+    T, Hkv, D = key.shape
+    NB, Hkv2, bs, D2 = key_cache.shape
+    if value.shape != key.shape or value_cache.shape != key_cache.shape or (Hkv2, D2) != (Hkv, D):
+        raise ValueError("reshape_and_cache: inconsistent shapes")
+    if slot_mapping.shape != (T,):
+        raise ValueError("reshape_and_cache: slot_mapping must be [num_tokens]")
+    dt = _dt(key)
+    for t, n in ((value, "value"), (key_cache, "key_cache"), (value_cache, "value_cache")):
+        if t.dtype != key.dtype:
+            raise TypeError(f"{n} dtype differs from key")
+    _check(_lib.pa_reshape_and_cache(
+        _dev(key, "key"), _dev(value, "value"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(slot_mapping, "slot_mapping", torch.int32),
+        T, Hkv, D, bs, NB, dt, _opt_dev(status, "status"), _stream(stream)))
+
+
+def _decode_common(out, query, key_cache, value_cache, block_tables, context_lens):
+    import torch
+    S, Hq, D = query.shape
+    NB, Hkv, bs, D2 = key_cache.shape
+    if out.shape != query.shape or value_cache.shape != key_cache.shape or D2 != D:
+        raise ValueError("decode: inconsistent shapes")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("decode: block_tables [S, max_blocks] and context_lens [S] expected")
+    dt = _dt(query)
+    for t, n in ((out, "out"), (key_cache, "key_cache"), (value_cache, "value_cache")):
+        if t.dtype != query.dtype:
+            raise TypeError(f"{n} dtype differs from query")
+    ptrs = (_dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+            int(block_tables.shape[1]), _dev(context_lens, "context_lens", torch.int32))
+    return ptrs, (S, Hq, Hkv, D, bs, NB), dt
+
+
+def pa_decode_v1(out, query, key_cache, value_cache, block_tables, context_lens,
+                 max_context_len: int, scale: float, status=None, stream=None):
+    ptrs, (S, Hq, Hkv, D, bs, NB), dt = _decode_common(out, query, key_cache, value_cache,
+                                                       block_tables, context_lens)
+    _check(_lib.pa_decode_v1(*ptrs, S, Hq, Hkv, D, bs, NB, int(max_context_len), float(scale), dt,
+                             _opt_dev(status, "status"), _stream(stream)))
+
+
+def pa_decode_v2_workspace_size(num_seqs, num_q_heads, head_size, max_context_len,
+                                partition_size) -> int:
+    return int(_lib.pa_decode_v2_workspace_size(num_seqs, num_q_heads, head_size,
+                                                max_context_len, partition_size))
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def pa_decode_v2(out, query, key_cache, value_cache, block_tables, context_lens,
+                 max_context_len: int, scale: float, partition_size: int, workspace,
+                 status=None, stream=None):
+    ptrs, (S, Hq, Hkv, D, bs, NB), dt = _decode_common(out, query, key_cache, value_cache,
+                                                       block_tables, context_lens)
+    wp, wb = _ws(workspace)
+    _check(_lib.pa_decode_v2(*ptrs, S, Hq, Hkv, D, bs, NB, int(max_context_len), float(scale), dt,
+                             int(partition_size), wp, wb, _opt_dev(status, "status"),
+                             _stream(stream)))
+
+
+def pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                        max_context_len):
+    v, p = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(_lib.pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                    max_context_len, ctypes.byref(v), ctypes.byref(p)))
+    return int(v.value), int(p.value)
+
+
+def pa_decode_auto_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                  max_context_len) -> int:
+    return int(_lib.pa_decode_auto_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                                  block_size, max_context_len))
+
+
+def pa_decode_auto(out, query, key_cache, value_cache, block_tables, context_lens,
+                   max_context_len: int, scale: float, workspace=None, status=None, stream=None):
+    ptrs, (S, Hq, Hkv, D, bs, NB), dt = _decode_common(out, query, key_cache, value_cache,
+                                                       block_tables, context_lens)
+    wp, wb = _ws(workspace)
+    _check(_lib.pa_decode_auto(*ptrs, S, Hq, Hkv, D, bs, NB, int(max_context_len), float(scale),
+                               dt, wp, wb, _opt_dev(status, "status"), _stream(stream)))
+
+
+def pa_decode_step(out, query, key, value, key_cache, value_cache, slot_mapping, block_tables,
+                   context_lens, max_context_len: int, scale: float, workspace=None, status=None,
+                   stream=None):
+    import torch
+    S, Hq, D = query.shape
+    NB, Hkv, bs, D2 = key_cache.shape
+    if key.shape != (S, Hkv, D) or value.shape != key.shape or slot_mapping.shape != (S,):
+        raise ValueError("decode_step: key/value [S, Hkv, D] and slot_mapping [S] expected")
+    if out.shape != query.shape or value_cache.shape != key_cache.shape or D2 != D:
+        raise ValueError("decode_step: inconsistent shapes")
+    dt = _dt(query)
+    wp, wb = _ws(workspace)
+    _check(_lib.pa_decode_step(
+        _dev(out, "out"), _dev(query, "query"), _dev(key, "key"), _dev(value, "value"),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(slot_mapping, "slot_mapping", torch.int32),
+        _dev(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
+        _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, D, bs, NB,
+        int(max_context_len), float(scale), dt, wp, wb, _opt_dev(status, "status"),
+        _stream(stream)))
+
+
+def pa_set_kernel_events(start_event, stop_event):
+    """torch.cuda.Event pair (already recorded once, so that the CUDA event exists) or
+    (None, None) to switch the hook off."""
+    if start_event is None or stop_event is None:
+        _check(_lib.pa_set_kernel_events(None, None))
+        return
+    _check(_lib.pa_set_kernel_events(ctypes.c_void_p(start_event.cuda_event),
+                                     ctypes.c_void_p(stop_event.cuda_event)))
+
+
+def pa_set_gqa_tensor_cores(enable: bool):
+    _check(_lib.pa_set_gqa_tensor_cores(1 if enable else 0))
+
+
+# --------------------------------------------------------------------------- allocator
+def _np_i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _nptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class PagedAllocator:
+    """Host block allocator (pa_alloc_* calls): builds block tables and slot mappings."""
+
+    def __init__(self, num_blocks: int, block_size: int, seed: int):
+        h = ctypes.c_void_p()
+        _check(_lib.pa_alloc_create(int(num_blocks), int(block_size),
+                                    int(seed) & (2**64 - 1), ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if self._h:
+            _lib.pa_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free(self) -> int:
+        return int(_lib.pa_alloc_num_free(self._h))
+
+    def pa_alloc_add_seq(self, seq_id: int, num_tokens: int):
+        _check(_lib.pa_alloc_add_seq(self._h, int(seq_id), int(num_tokens)))
+
+    def pa_alloc_append(self, seq_id: int) -> int:
+        s = ctypes.c_int32(0)
+        _check(_lib.pa_alloc_append(self._h, int(seq_id), ctypes.byref(s)))
+        return int(s.value)
+
+    def pa_alloc_append_batch(self, seq_ids) -> np.ndarray:
+        ids = _np_i32(seq_ids)
+        out = np.empty(ids.size, dtype=np.int32)
+        _check(_lib.pa_alloc_append_batch(self._h, _nptr(ids), ids.size, _nptr(out)))
+        return out
+
+    def pa_alloc_free_seq(self, seq_id: int):
+        _check(_lib.pa_alloc_free_seq(self._h, int(seq_id)))
+
+    def pa_alloc_slots(self, seq_id: int, start: int, n: int) -> np.ndarray:
+        out = np.empty(int(n), dtype=np.int32)
+        _check(_lib.pa_alloc_slots(self._h, int(seq_id), int(start), int(n), _nptr(out)))
+        return out
+
+    def pa_alloc_block_tables(self, seq_ids, max_blocks_per_seq: int) -> np.ndarray:
+        ids = _np_i32(seq_ids)
+        out = np.empty((ids.size, int(max_blocks_per_seq)), dtype=np.int32)
+        _check(_lib.pa_alloc_block_tables(self._h, _nptr(ids), ids.size, int(max_blocks_per_seq),
+                                          _nptr(out)))
+        return out
+
+    def pa_alloc_context_lens(self, seq_ids) -> np.ndarray:
+        ids = _np_i32(seq_ids)
+        out = np.empty(ids.size, dtype=np.int32)
+        _check(_lib.pa_alloc_context_lens(self._h, _nptr(ids), ids.size, _nptr(out)))
+        return out

@@ -1,0 +1,651 @@
+// pa_host.cpp -- host side of the C ABI declared in include/pa.h: argument checks,
+// TMA tensor-map encoding, V1 / V2 / auto dispatch, and the host block allocator.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+pa_status ok() {
+    g_last_error.clear();
+    return PA_OK;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ device facts
+struct DeviceInfo {
+    int sms = 0;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceInfo> g_dev;
+std::unordered_map<uint64_t, int32_t> g_occ;   // (device, kernel key) -> CTAs per SM
+int32_t g_gqa_mma = 1;
+cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+
+// Launches the decode kernel, bracketed by the profiling events when they are set.
+cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
+                         const pa::DecodeParams& p, bool persistent, int32_t units,
+                         cudaStream_t st);
+
+pa_status current_device(int* dev, DeviceInfo* info) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(*dev);
+    if (it == g_dev.end()) {
+        DeviceInfo di;
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, *dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        it = g_dev.emplace(*dev, di).first;
+    }
+    *info = it->second;
+    return PA_OK;
+}
+
+cudaError_t dispatch_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
+                            const pa::DecodeParams& p, bool persistent, int32_t units,
+                            cudaStream_t st, int32_t* occ) {
+    if (k.head_size == 128)
+        return k.bf16 ? pa::launch_decode_bf16_d128(k, km, vm, p, persistent, units, st, occ)
+                      : pa::launch_decode_f16_d128(k, km, vm, p, persistent, units, st, occ);
+    return k.bf16 ? pa::launch_decode_bf16_d64(k, km, vm, p, persistent, units, st, occ)
+                  : pa::launch_decode_f16_d64(k, km, vm, p, persistent, units, st, occ);
+}
+
+cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
+                         const pa::DecodeParams& p, bool persistent, int32_t units,
+                         cudaStream_t st) {
+    cudaEvent_t a = g_ev_start, b = g_ev_stop;
+    if (a && b) {
+        cudaError_t e = cudaEventRecord(a, st);
+        if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = dispatch_decode(k, km, vm, p, persistent, units, st, nullptr);
+    if (e == cudaSuccess && a && b) e = cudaEventRecord(b, st);
+    return e;
+}
+
+int32_t ctas_per_sm(int dev, const pa::KernelKey& k) {
+    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)(k.head_size == 128) << 20 |
+                         (uint64_t)(k.block_size == 32) << 19 | (uint64_t)k.bf16 << 18 |
+                         (uint64_t)k.mma << 17 | (uint64_t)k.heads_cap;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    CUtensorMap dummy;
+    std::memset(&dummy, 0, sizeof(dummy));
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    int32_t n = 0;
+    if (dispatch_decode(k, dummy, dummy, p, true, 0, nullptr, &n) != cudaSuccess) n = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ[key] = n;
+    return n;
+}
+
+// ------------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The pool [num_blocks][num_kv_heads][block_size][head_size] viewed as a 2-D matrix of
+// rows = num_blocks*num_kv_heads*block_size and head_size columns; a box is 64 columns
+// (128 bytes, the swizzle span) by block_size rows, i.e. one half of a (block, head)
+// tile when head_size is 128.
+pa_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int32_t head_size,
+                          int32_t block_size) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_size * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(pool), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PA_OK;
+}
+
+// ------------------------------------------------------------------ argument checks
+struct DecodeArgs {
+    void* out;
+    const void* query;
+    const void* key_cache;
+    const void* value_cache;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    int32_t num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks;
+    int32_t max_context_len;
+    float scale;
+    pa_dtype dtype;
+    int32_t* status;
+    cudaStream_t stream;
+};
+
+pa_status check_decode(const DecodeArgs& a) {
+    if (a.num_seqs < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_blocks <= 0 ||
+        a.max_blocks_per_seq <= 0 || a.max_context_len < 0)
+        return fail(PA_ERR_INVALID_ARG, "decode: sizes must be positive (num_seqs >= 0)");
+    if (a.dtype != PA_F16 && a.dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "decode: dtype");
+    if (a.head_size != 64 && a.head_size != 128)
+        return fail(PA_ERR_UNSUPPORTED, "decode: head_size %d (64 or 128)", a.head_size);
+    if (a.block_size != 16 && a.block_size != 32)
+        return fail(PA_ERR_UNSUPPORTED, "decode: block_size %d (16 or 32)", a.block_size);
+    if (a.num_q_heads % a.num_kv_heads)
+        return fail(PA_ERR_INVALID_ARG, "decode: num_q_heads %% num_kv_heads != 0");
+    if (a.num_q_heads / a.num_kv_heads > 16)
+        return fail(PA_ERR_UNSUPPORTED, "decode: query group %d > 16",
+                    a.num_q_heads / a.num_kv_heads);
+    const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
+    if (rows + (int64_t)a.num_kv_heads * a.block_size > INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "decode: pool has more than 2^31 rows");
+    if (a.num_seqs == 0) return PA_OK;
+    if (!a.out || !a.query || !a.key_cache || !a.value_cache || !a.block_tables || !a.context_lens)
+        return fail(PA_ERR_INVALID_ARG, "decode: null pointer");
+    if (!aligned16(a.out) || !aligned16(a.query) || !aligned16(a.key_cache) ||
+        !aligned16(a.value_cache))
+        return fail(PA_ERR_INVALID_ARG, "decode: device buffers must be 16-byte aligned");
+    return PA_OK;
+}
+
+pa::KernelKey kernel_key(const DecodeArgs& a) {
+    pa::KernelKey k;
+    k.head_size = a.head_size;
+    k.block_size = a.block_size;
+    k.bf16 = a.dtype == PA_BF16;
+    const int g = a.num_q_heads / a.num_kv_heads;
+    k.mma = g >= 2 && (g > 8 || g_gqa_mma);
+    if (k.mma) k.heads_cap = g <= 8 ? 8 : 16;
+    else k.heads_cap = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
+    return k;
+}
+
+pa::DecodeParams base_params(const DecodeArgs& a) {
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.out = a.out;
+    p.q = a.query;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.max_blocks_per_seq = a.max_blocks_per_seq;
+    p.num_seqs = a.num_seqs;
+    p.num_q_heads = a.num_q_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.group = a.num_q_heads / a.num_kv_heads;
+    p.num_blocks = a.num_blocks;
+    p.block_size = a.block_size;
+    p.max_context_len = a.max_context_len;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.status = a.status;
+    return p;
+}
+
+pa_status make_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+    const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
+    pa_status st = encode_pool_map(km, a.key_cache, rows, a.head_size, a.block_size);
+    if (st != PA_OK) return st;
+    return encode_pool_map(vm, a.value_cache, rows, a.head_size, a.block_size);
+}
+
+pa_status run_v1(const DecodeArgs& a) {
+    pa_status st = check_decode(a);
+    if (st != PA_OK || a.num_seqs == 0) return st == PA_OK ? ok() : st;
+    CUtensorMap km, vm;
+    if ((st = make_maps(a, &km, &vm)) != PA_OK) return st;
+    pa::DecodeParams p = base_params(a);
+    p.partition_size = 0;
+    const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads;
+    if (units > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "decode_v1: too many (seq, head) units");
+    cudaError_t e = timed_decode(kernel_key(a), km, vm, p, false, (int32_t)units, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_v1 launch");
+    return ok();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t ws_bytes) {
+    pa_status st = check_decode(a);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % a.block_size)
+        return fail(PA_ERR_INVALID_ARG, "decode_v2: partition_size %d must be a positive multiple "
+                    "of block_size %d", partition_size, a.block_size);
+    if (a.num_seqs == 0) return ok();
+    const pa::WorkspaceLayout L = pa::v2_workspace_layout(a.num_seqs, a.num_q_heads, a.head_size,
+                                                          a.max_context_len, partition_size);
+    if (!ws || ws_bytes < L.total)
+        return fail(PA_ERR_WORKSPACE, "decode_v2: workspace of %zu bytes, need %zu", ws_bytes, L.total);
+    if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return fail(PA_ERR_INVALID_ARG, "decode_v2: workspace must be 256-byte aligned");
+    int dev;
+    DeviceInfo di;
+    if ((st = current_device(&dev, &di)) != PA_OK) return st;
+    CUtensorMap km, vm;
+    if ((st = make_maps(a, &km, &vm)) != PA_OK) return st;
+    pa::DecodeParams p = base_params(a);
+    p.partition_size = partition_size;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.hdr = reinterpret_cast<pa::WsHeader*>(w + L.hdr);
+    p.part_offset = reinterpret_cast<int32_t*>(w + L.part_offset);
+    p.part_list = reinterpret_cast<int2*>(w + L.part_list);
+    p.part_ml = reinterpret_cast<float2*>(w + L.part_ml);
+    p.part_acc = reinterpret_cast<float*>(w + L.part_acc);
+    const pa::KernelKey k = kernel_key(a);
+    const int32_t per_sm = ctas_per_sm(dev, k);
+    if (per_sm <= 0) return fail(PA_ERR_CUDA, "decode_v2: kernel cannot be resident on this device");
+    const int64_t max_parts_per_seq =
+        std::max<int64_t>(1, ((int64_t)a.max_context_len + partition_size - 1) / partition_size);
+    const int64_t max_units = (int64_t)a.num_seqs * max_parts_per_seq * a.num_kv_heads;
+    const int32_t grid = (int32_t)std::min<int64_t>((int64_t)per_sm * di.sms, max_units);
+    cudaError_t e = pa::launch_plan(p, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_v2 plan launch");
+    e = timed_decode(k, km, vm, p, true, grid, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_v2 launch");
+    if (a.max_context_len > partition_size) {   // some sequence may span several partitions
+        e = pa::launch_reduce(p, a.head_size, k.bf16, a.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_v2 reduce launch");
+    }
+    return ok();
+}
+
+// pa_decode_auto's choice.  V1 gives a whole context to one work unit, which is fine
+// while every context is short and there are many units; otherwise V2 splits contexts
+// into partitions that the persistent CTAs share out.
+void auto_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t block_size,
+               int32_t max_context_len, int32_t* variant, int32_t* psize) {
+    int dev = 0;
+    DeviceInfo di;
+    if (current_device(&dev, &di) != PA_OK || di.sms <= 0) di.sms = 148;
+    const int64_t units = (int64_t)num_seqs * num_kv_heads;
+    if (max_context_len <= 256 && units >= 4LL * di.sms) {
+        *variant = 1;
+        *psize = 0;
+        return;
+    }
+    int32_t P = 512;
+    // Keep at least ~8 units per SM so the last wave is short.
+    while (P > 2 * block_size && P > 64 &&
+           units * std::max<int64_t>(1, (max_context_len + P - 1) / P) < 8LL * di.sms)
+        P /= 2;
+    P = std::max(block_size, (P / block_size) * block_size);
+    *variant = 2;
+    *psize = P;
+}
+
+}  // namespace
+
+namespace pa {
+
+WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                    int32_t max_context_len, int32_t partition_size) {
+    WorkspaceLayout L;
+    const int64_t ppseq =
+        std::max<int64_t>(1, ((int64_t)std::max(max_context_len, 0) + partition_size - 1) / partition_size);
+    const int64_t parts = (int64_t)num_seqs * ppseq;
+    size_t off = 0;
+    L.hdr = off;
+    off = align256(off + sizeof(WsHeader));
+    L.part_offset = off;
+    off = align256(off + sizeof(int32_t) * (size_t)(num_seqs + 1));
+    L.part_list = off;
+    off = align256(off + sizeof(int2) * (size_t)parts);
+    L.part_ml = off;
+    off = align256(off + sizeof(float2) * (size_t)parts * (size_t)num_q_heads);
+    L.part_acc = off;
+    off = align256(off + sizeof(float) * (size_t)parts * (size_t)num_q_heads * (size_t)head_size);
+    L.total = off;
+    return L;
+}
+
+}  // namespace pa
+
+// =====================================================================================
+// C ABI
+// =====================================================================================
+extern "C" {
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+int32_t pa_version(void) { return 100; }
+
+pa_status pa_set_kernel_events(void* start_event, void* stop_event) {
+    if ((start_event == nullptr) != (stop_event == nullptr))
+        return fail(PA_ERR_INVALID_ARG, "set_kernel_events: give both events or neither");
+    g_ev_start = static_cast<cudaEvent_t>(start_event);
+    g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+    return ok();
+}
+
+pa_status pa_set_gqa_tensor_cores(int32_t enable) {
+    g_gqa_mma = enable ? 1 : 0;
+    return ok();
+}
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                               void* value_cache, const int32_t* slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                               int32_t num_blocks, pa_dtype dtype, int32_t* status_dev,
+                               pa_stream stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: sizes must be positive");
+    if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: dtype");
+    if (head_size % 8)
+        return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: head_size must be a multiple of 8");
+    if (num_tokens == 0) return ok();
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: buffers must be 16-byte aligned");
+    cudaError_t e = pa::launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
+                                                 num_tokens, num_kv_heads, head_size, block_size,
+                                                 num_blocks, status_dev, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+    return ok();
+}
+
+pa_status pa_decode_v1(void* out, const void* query, const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                       int32_t num_blocks, int32_t max_context_len, float scale, pa_dtype dtype,
+                       int32_t* status_dev, pa_stream stream) {
+    DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                 num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    return run_v1(a);
+}
+
+size_t pa_decode_v2_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                   int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || partition_size <= 0) return 0;
+    return pa::v2_workspace_layout(num_seqs, num_q_heads, head_size, max_context_len,
+                                   partition_size).total;
+}
+
+pa_status pa_decode_v2(void* out, const void* query, const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                       int32_t num_blocks, int32_t max_context_len, float scale, pa_dtype dtype,
+                       int32_t partition_size, void* workspace, size_t workspace_bytes,
+                       int32_t* status_dev, pa_stream stream) {
+    DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                 num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    return run_v2(a, partition_size, workspace, workspace_bytes);
+}
+
+pa_status pa_decode_auto_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, int32_t block_size, int32_t max_context_len,
+                              int32_t* variant, int32_t* partition_size) {
+    (void)num_q_heads;
+    (void)head_size;
+    if (!variant || !partition_size) return fail(PA_ERR_INVALID_ARG, "auto_plan: null output");
+    if (num_seqs < 0 || num_kv_heads <= 0 || block_size <= 0 || max_context_len < 0)
+        return fail(PA_ERR_INVALID_ARG, "auto_plan: bad sizes");
+    auto_plan(num_seqs, num_kv_heads, block_size, max_context_len, variant, partition_size);
+    return ok();
+}
+
+size_t pa_decode_auto_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_size, int32_t block_size,
+                                     int32_t max_context_len) {
+    int32_t v = 0, P = 0;
+    if (pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                            max_context_len, &v, &P) != PA_OK)
+        return 0;
+    if (v == 1) return 0;
+    return pa_decode_v2_workspace_size(num_seqs, num_q_heads, head_size, max_context_len, P);
+}
+
+pa_status pa_decode_auto(void* out, const void* query, const void* key_cache,
+                         const void* value_cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                         int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                         float scale, pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, pa_stream stream) {
+    int32_t v = 0, P = 0;
+    pa_status st = pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                       max_context_len, &v, &P);
+    if (st != PA_OK) return st;
+    DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                 num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    if (v == 1) return run_v1(a);
+    return run_v2(a, P, workspace, workspace_bytes);
+}
+
+pa_status pa_decode_step(void* out, const void* query, const void* key, const void* value,
+                         void* key_cache, void* value_cache, const int32_t* slot_mapping,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                         int32_t num_blocks, int32_t max_context_len, float scale, pa_dtype dtype,
+                         void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                         pa_stream stream) {
+    pa_status st = pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, num_seqs,
+                                        num_kv_heads, head_size, block_size, num_blocks, dtype,
+                                        status_dev, stream);
+    if (st != PA_OK) return st;
+    return pa_decode_auto(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                          context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                          num_blocks, max_context_len, scale, dtype, workspace, workspace_bytes,
+                          status_dev, stream);
+}
+
+}  // extern "C"
+
+// =====================================================================================
+// Host block allocator
+// =====================================================================================
+struct pa_alloc {
+    int32_t num_blocks = 0;
+    int32_t block_size = 0;
+    std::vector<int32_t> free_list;   // popped from the back
+    struct Seq {
+        std::vector<int32_t> blocks;
+        int32_t len = 0;
+    };
+    std::unordered_map<int32_t, Seq> seqs;
+};
+
+namespace {
+
+// splitmix64 (Steele, Lea and Flood, OOPSLA 2014).
+uint64_t splitmix64(uint64_t& s) {
+    s += 0x9E3779B97F4A7C15ull;
+    uint64_t z = s;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed, pa_alloc** out) {
+    if (!out) return fail(PA_ERR_INVALID_ARG, "alloc_create: null output");
+    *out = nullptr;
+    if (num_blocks <= 0 || block_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "alloc_create: num_blocks and block_size must be positive");
+    if ((int64_t)num_blocks * block_size > INT32_MAX)
+        return fail(PA_ERR_INVALID_ARG, "alloc_create: num_blocks * block_size overflows int32 slots");
+    auto* a = new pa_alloc;
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->free_list.resize(num_blocks);
+    for (int32_t i = 0; i < num_blocks; ++i) a->free_list[i] = i;
+    uint64_t st = seed;
+    for (int32_t i = num_blocks - 1; i >= 1; --i) {
+        const int32_t j = (int32_t)(splitmix64(st) % (uint64_t)(i + 1));
+        std::swap(a->free_list[i], a->free_list[j]);
+    }
+    *out = a;
+    return ok();
+}
+
+void pa_alloc_destroy(pa_alloc* a) { delete a; }
+
+int32_t pa_alloc_num_free(const pa_alloc* a) { return a ? (int32_t)a->free_list.size() : 0; }
+
+pa_status pa_alloc_add_seq(pa_alloc* a, int32_t seq_id, int32_t num_tokens) {
+    if (!a || seq_id < 0 || num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "alloc_add_seq: bad args");
+    if (a->seqs.count(seq_id)) return fail(PA_ERR_INVALID_ARG, "alloc_add_seq: seq %d is live", seq_id);
+    const int64_t need = ((int64_t)num_tokens + a->block_size - 1) / a->block_size;
+    if (need > (int64_t)a->free_list.size())
+        return fail(PA_ERR_NO_BLOCKS, "alloc_add_seq: need %lld blocks, %zu free", (long long)need,
+                    a->free_list.size());
+    pa_alloc::Seq s;
+    s.len = num_tokens;
+    s.blocks.reserve(need);
+    for (int64_t i = 0; i < need; ++i) {
+        s.blocks.push_back(a->free_list.back());
+        a->free_list.pop_back();
+    }
+    a->seqs.emplace(seq_id, std::move(s));
+    return ok();
+}
+
+pa_status pa_alloc_append(pa_alloc* a, int32_t seq_id, int32_t* slot_out) {
+    if (!a || !slot_out) return fail(PA_ERR_INVALID_ARG, "alloc_append: null argument");
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_append: unknown seq %d", seq_id);
+    pa_alloc::Seq& s = it->second;
+    if (s.len % a->block_size == 0) {
+        if (a->free_list.empty()) return fail(PA_ERR_NO_BLOCKS, "alloc_append: no free block");
+        s.blocks.push_back(a->free_list.back());
+        a->free_list.pop_back();
+    }
+    *slot_out = s.blocks[s.len / a->block_size] * a->block_size + s.len % a->block_size;
+    s.len += 1;
+    return ok();
+}
+
+pa_status pa_alloc_append_batch(pa_alloc* a, const int32_t* seq_ids, int32_t n, int32_t* slots_out) {
+    if (!a || n < 0 || (n > 0 && (!seq_ids || !slots_out)))
+        return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: bad args");
+    int64_t need = 0;
+    std::unordered_set<int32_t> seen;
+    seen.reserve((size_t)n * 2);
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end())
+            return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: unknown seq %d", seq_ids[i]);
+        if (!seen.insert(seq_ids[i]).second)
+            return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: seq %d listed twice", seq_ids[i]);
+        if (it->second.len % a->block_size == 0) ++need;
+    }
+    if (need > (int64_t)a->free_list.size())
+        return fail(PA_ERR_NO_BLOCKS, "alloc_append_batch: need %lld blocks, %zu free",
+                    (long long)need, a->free_list.size());
+    for (int32_t i = 0; i < n; ++i) {
+        pa_status st = pa_alloc_append(a, seq_ids[i], &slots_out[i]);
+        if (st != PA_OK) return st;
+    }
+    return ok();
+}
+
+pa_status pa_alloc_free_seq(pa_alloc* a, int32_t seq_id) {
+    if (!a) return fail(PA_ERR_INVALID_ARG, "alloc_free_seq: null handle");
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_free_seq: unknown seq %d", seq_id);
+    for (int32_t b : it->second.blocks) a->free_list.push_back(b);
+    a->seqs.erase(it);
+    return ok();
+}
+
+pa_status pa_alloc_slots(const pa_alloc* a, int32_t seq_id, int32_t start, int32_t n, int32_t* out) {
+    if (!a || (n > 0 && !out) || start < 0 || n < 0) return fail(PA_ERR_INVALID_ARG, "alloc_slots: bad args");
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_slots: unknown seq %d", seq_id);
+    const pa_alloc::Seq& s = it->second;
+    if ((int64_t)start + n > s.len) return fail(PA_ERR_INVALID_ARG, "alloc_slots: past the sequence end");
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t t = start + i;
+        out[i] = s.blocks[t / a->block_size] * a->block_size + t % a->block_size;
+    }
+    return ok();
+}
+
+pa_status pa_alloc_block_tables(const pa_alloc* a, const int32_t* seq_ids, int32_t n,
+                                int32_t max_blocks_per_seq, int32_t* out) {
+    if (!a || n < 0 || max_blocks_per_seq <= 0 || (n > 0 && (!seq_ids || !out)))
+        return fail(PA_ERR_INVALID_ARG, "alloc_block_tables: bad args");
+    for (int32_t r = 0; r < n; ++r) {
+        auto it = a->seqs.find(seq_ids[r]);
+        if (it == a->seqs.end())
+            return fail(PA_ERR_INVALID_ARG, "alloc_block_tables: unknown seq %d", seq_ids[r]);
+        const std::vector<int32_t>& b = it->second.blocks;
+        if ((int64_t)b.size() > max_blocks_per_seq)
+            return fail(PA_ERR_INVALID_ARG, "alloc_block_tables: seq %d has %zu blocks > %d",
+                        seq_ids[r], b.size(), max_blocks_per_seq);
+        int32_t* row = out + (size_t)r * max_blocks_per_seq;
+        std::copy(b.begin(), b.end(), row);
+        std::fill(row + b.size(), row + max_blocks_per_seq, -1);
+    }
+    return ok();
+}
+
+pa_status pa_alloc_context_lens(const pa_alloc* a, const int32_t* seq_ids, int32_t n, int32_t* out) {
+    if (!a || n < 0 || (n > 0 && (!seq_ids || !out)))
+        return fail(PA_ERR_INVALID_ARG, "alloc_context_lens: bad args");
+    for (int32_t r = 0; r < n; ++r) {
+        auto it = a->seqs.find(seq_ids[r]);
+        if (it == a->seqs.end())
+            return fail(PA_ERR_INVALID_ARG, "alloc_context_lens: unknown seq %d", seq_ids[r]);
+        out[r] = it->second.len;
+    }
+    return ok();
+}
+
+}  // extern "C"

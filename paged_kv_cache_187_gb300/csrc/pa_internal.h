@@ -1,0 +1,85 @@
+// pa_internal.h -- interface between the host side of the C ABI (pa_host.cpp) and the
+// kernel launchers (pa_decode_*.cu, pa_reshape.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Head of the V2 workspace.  The plan kernel writes it; the decode kernel's persistent
+// CTAs claim work units from `counter`.
+struct WsHeader {
+    uint32_t counter;      // next unclaimed work unit
+    uint32_t total_units;  // partitions * num_kv_heads
+    uint32_t total_parts;  // partitions over all sequences
+    uint32_t pad[61];
+};
+
+struct DecodeParams {
+    void* out;                    // [S][Hq][D] of the dtype
+    const void* q;                // [S][Hq][D]
+    const int32_t* block_tables;  // [S][max_blocks_per_seq]
+    const int32_t* context_lens;  // [S]
+    int32_t max_blocks_per_seq;
+    int32_t num_seqs, num_q_heads, num_kv_heads, group;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t max_context_len;
+    float scale_log2;             // softmax scale * log2(e): logits live in base-2 units
+    int32_t partition_size;       // tokens per work unit; 0 = the whole context (V1)
+    // V2 workspace pieces (null for V1)
+    WsHeader* hdr;
+    int32_t* part_offset;         // [S + 1] first partition index of each sequence
+    int2* part_list;              // [parts] (sequence, partition) of each partition
+    float* part_acc;              // [parts][Hq][D] unnormalised partial outputs
+    float2* part_ml;              // [parts][Hq] (running max in base-2 units, exp-sum)
+    int32_t* status;              // optional device error word
+};
+
+struct WorkspaceLayout {
+    size_t hdr, part_offset, part_list, part_ml, part_acc, total;
+};
+
+WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                    int32_t max_context_len, int32_t partition_size);
+
+// Selects the kernel instantiation.
+struct KernelKey {
+    int32_t head_size;   // 64 | 128
+    int32_t block_size;  // 16 | 32
+    bool bf16;
+    bool mma;            // tensor-core path (group >= 2) or CUDA-core path
+    int32_t heads_cap;   // mma: 8 or 16 (n-tiles * 8); CUDA cores: 1, 2, 4 or 8
+};
+
+// Launchers return cudaSuccess or the launch error.  `persistent` selects the V2
+// schedule (grid = resident CTAs, units claimed from the workspace counter).
+cudaError_t launch_decode(const KernelKey& key, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const DecodeParams& p, bool persistent, int32_t num_units,
+                          cudaStream_t stream);
+cudaError_t launch_plan(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_reduce(const DecodeParams& p, int32_t head_size, bool bf16,
+                          cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                     void* value_cache, const int32_t* slot_mapping,
+                                     int32_t num_tokens, int32_t num_kv_heads,
+                                     int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                     int32_t* status, cudaStream_t stream);
+
+// Resident CTAs per SM of a decode instantiation (0 if it cannot launch).
+int32_t decode_ctas_per_sm(const KernelKey& key);
+
+// Per-instantiation family launchers, one per translation unit.
+cudaError_t launch_decode_f16_d128(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                   const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_bf16_d128(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                    const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_f16_d64(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                  const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_bf16_d64(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                   const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+
+}  // namespace pa

@@ -1,0 +1,147 @@
+"""A decode batch resident on the GPU, driven through the C ABI.
+
+``DecodeRunner`` is the serving loop of one attention layer for a synthetic workload:
+  1. the host allocator ("[core] Multi Step Scheduling #7000": the v2 block manager
+     hands out blocks and the slot_mapping / block_tables / seq_lens metadata) places
+     every sequence's prefill tokens, and pa_reshape_and_cache writes their K/V rows
+     into NaN-poisoned pools;
+  2. each decode step appends one token per sequence on the host (pa_alloc_append_batch),
+     copies the step's metadata to the device, scatters the new K/V rows and runs the
+     decode (pa_decode_step = reshape_and_cache + pa_decode_auto), or a chosen variant.
+
+torch provides device memory and streams only; every step of the path runs in
+libpa.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as B
+from . import workloads as W
+
+
+class DecodeRunner:
+    def __init__(self, w: W.Workload, device="cuda", rank: int = 0, poison: bool = True,
+                 prefill_chunk_tokens: int = 65536, start_lens=None, num_blocks=None,
+                 alloc_seed=None):
+        """``start_lens`` / ``num_blocks`` / ``alloc_seed`` override the workload's own
+        (first-step context lengths including the new token, pool size, allocator seed)."""
+        self.w = w
+        self.device = torch.device(device)
+        self.rank = rank
+        S, bs = w.num_seqs, w.block_size
+        self.start_lens = (W.start_context_lens(w) if start_lens is None
+                           else np.asarray(start_lens, dtype=np.int32))
+        assert self.start_lens.shape == (S,) and int(self.start_lens.min()) >= 1
+        self.num_blocks = (W.pool_blocks(w, self.start_lens) if num_blocks is None
+                           else int(num_blocks))
+        self.alloc_seed = (w.seed + rank) if alloc_seed is None else int(alloc_seed)
+        self.max_blocks = W.max_blocks_per_seq(w, self.start_lens)
+        self.max_context_len = int(self.start_lens.max()) + w.steps - 1
+        self.tdtype = W.torch_dtype(w)
+        self.alloc = B.PagedAllocator(self.num_blocks, bs, seed=self.alloc_seed)
+        self.seq_ids = np.arange(S, dtype=np.int32)
+        self.prefill_lens = (self.start_lens - 1).astype(np.int64)
+        for s in range(S):
+            self.alloc.pa_alloc_add_seq(s, int(self.prefill_lens[s]))
+        shape = (self.num_blocks, w.num_kv_heads, bs, w.head_size)
+        self.key_cache = torch.empty(shape, dtype=self.tdtype, device=self.device)
+        self.value_cache = torch.empty(shape, dtype=self.tdtype, device=self.device)
+        if poison:
+            nan = W.NAN_BITS[w.dtype]
+            nan = nan - 65536 if nan >= 32768 else nan
+            self.key_cache.view(torch.int16).fill_(nan)
+            self.value_cache.view(torch.int16).fill_(nan)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        # prefill: tokens in sequence order, positions 0 .. L-2 of every sequence
+        self.prefill_offsets = np.concatenate([[0], np.cumsum(self.prefill_lens)]).astype(np.int64)
+        total = int(self.prefill_offsets[-1])
+        self.k_prefill = W.randn_16bit((total, w.num_kv_heads, w.head_size), w.dtype,
+                                       W.stream_seed(w, "k_prefill", 0, rank), self.device)
+        self.v_prefill = W.randn_16bit((total, w.num_kv_heads, w.head_size), w.dtype,
+                                       W.stream_seed(w, "v_prefill", 0, rank), self.device)
+        slots = np.concatenate([self.alloc.pa_alloc_slots(s, 0, int(self.prefill_lens[s]))
+                                for s in range(S)] + [np.zeros(0, np.int32)])
+        self.prefill_slots = slots
+        slots_d = torch.from_numpy(slots).to(self.device)
+        for i in range(0, total, prefill_chunk_tokens):
+            j = min(total, i + prefill_chunk_tokens)
+            B.pa_reshape_and_cache(self.k_prefill[i:j], self.v_prefill[i:j], self.key_cache,
+                                   self.value_cache, slots_d[i:j], status=self.status)
+        self.step_index = -1
+        self.out = torch.empty((S, w.num_q_heads, w.head_size), dtype=self.tdtype,
+                               device=self.device)
+        ws = max(B.pa_decode_auto_workspace_size(S, w.num_q_heads, w.num_kv_heads, w.head_size,
+                                                 bs, self.max_context_len),
+                 B.pa_decode_v2_workspace_size(S, w.num_q_heads, w.head_size,
+                                               self.max_context_len, w.partition_size), 256)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=self.device)
+
+    # ------------------------------------------------------------------ one step
+    def next_step(self):
+        """Host side of a decode step: append one token per sequence, build the
+        metadata, draw the step's q / k / v, and stage everything on the device."""
+        w = self.w
+        self.step_index += 1
+        k = self.step_index
+        self.slots = self.alloc.pa_alloc_append_batch(self.seq_ids)
+        self.block_tables = self.alloc.pa_alloc_block_tables(self.seq_ids, self.max_blocks)
+        self.context_lens = self.alloc.pa_alloc_context_lens(self.seq_ids)
+        self.slots_d = torch.from_numpy(self.slots).to(self.device)
+        self.block_tables_d = torch.from_numpy(self.block_tables).to(self.device)
+        self.context_lens_d = torch.from_numpy(self.context_lens).to(self.device)
+        S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
+        self.q = W.randn_16bit((S, Hq, D), w.dtype, W.stream_seed(w, "q", k, self.rank), self.device)
+        self.k_new = W.randn_16bit((S, Hkv, D), w.dtype, W.stream_seed(w, "k_new", k, self.rank),
+                                   self.device)
+        self.v_new = W.randn_16bit((S, Hkv, D), w.dtype, W.stream_seed(w, "v_new", k, self.rank),
+                                   self.device)
+        return self
+
+    def step_max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.context_lens.size else 0
+
+    def run_reshape(self, stream=None):
+        B.pa_reshape_and_cache(self.k_new, self.v_new, self.key_cache, self.value_cache,
+                               self.slots_d, status=self.status, stream=stream)
+
+    def run_decode(self, variant: str = "auto", partition_size: int | None = None, stream=None,
+                   max_context_len: int | None = None):
+        mcl = self.step_max_context_len() if max_context_len is None else max_context_len
+        args = (self.out, self.q, self.key_cache, self.value_cache, self.block_tables_d,
+                self.context_lens_d, mcl, self.w.scale)
+        if variant == "v1":
+            B.pa_decode_v1(*args, status=self.status, stream=stream)
+        elif variant == "v2":
+            P = partition_size or self.w.partition_size
+            need = B.pa_decode_v2_workspace_size(self.w.num_seqs, self.w.num_q_heads,
+                                                 self.w.head_size, mcl, P)
+            if need > self.workspace.numel():
+                self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+            B.pa_decode_v2(*args, P, self.workspace, status=self.status, stream=stream)
+        elif variant == "auto":
+            B.pa_decode_auto(*args, workspace=self.workspace, status=self.status, stream=stream)
+        else:
+            raise ValueError(variant)
+
+    def run_step(self, stream=None):
+        """reshape_and_cache + pa_decode_auto through the single pa_decode_step call."""
+        B.pa_decode_step(self.out, self.q, self.k_new, self.v_new, self.key_cache,
+                         self.value_cache, self.slots_d, self.block_tables_d, self.context_lens_d,
+                         self.step_max_context_len(), self.w.scale, workspace=self.workspace,
+                         status=self.status, stream=stream)
+
+    # ------------------------------------------------------------------ accounting
+    def kv_bytes(self) -> int:
+        """Algorithmic bytes of one decode step: every context token's K and V row of
+        every kv head, plus the query and output rows."""
+        w = self.w
+        elt = 2
+        lens = self.context_lens.astype(np.int64)
+        kv = int(lens.sum()) * w.num_kv_heads * w.head_size * 2 * elt
+        qo = 2 * w.num_seqs * w.num_q_heads * w.head_size * elt
+        return kv + qo
+
+    def seq_tokens(self) -> int:
+        return int(self.context_lens.astype(np.int64).sum())

@@ -1,0 +1,104 @@
+"""CPU-only checks of the C ABI library: it loads, exports every symbol include/pa.h
+declares, and its host block allocator matches the oracle allocator byte for byte
+(no GPU call is made here)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from paged_kv_cache_187_gb300 import build
+    build.build()
+    import paged_kv_cache_187_gb300 as pkg
+    return pkg
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "pa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared_functions()
+    for must in ("pa_reshape_and_cache", "pa_decode_v1", "pa_decode_v2", "pa_decode_auto",
+                 "pa_decode_v2_workspace_size", "pa_alloc_create", "pa_alloc_block_tables",
+                 "pa_alloc_append"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(pa):
+    lib = pa.raw()
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_workspace_size_is_host_only_and_monotone(pa):
+    a = pa.pa_decode_v2_workspace_size(256, 32, 128, 8192, 512)
+    b = pa.pa_decode_v2_workspace_size(256, 32, 128, 8192, 256)
+    assert 0 < a < b
+    # partials: parts * Hq * (D floats + (m, l)) dominate
+    parts = 256 * 16
+    assert a >= parts * 32 * (128 * 4 + 8)
+
+
+def test_auto_plan_choices(pa):
+    v, P = pa.pa_decode_auto_plan(256, 40, 40, 128, 16, 32768)
+    assert v == 2 and P % 16 == 0 and P > 0
+    v, P = pa.pa_decode_auto_plan(4096, 32, 8, 128, 16, 128)
+    assert v == 1 and P == 0
+    assert pa.pa_decode_auto_workspace_size(4096, 32, 8, 128, 16, 128) == 0
+
+
+@pytest.mark.parametrize("seed", [0, 1, 123456789, 2**63 + 5])
+def test_allocator_matches_oracle_allocator(pa, seed):
+    NB, bs = 97, 16
+    prod = pa.PagedAllocator(NB, bs, seed)
+    ref = oracle.Alloc(NB, bs, seed)
+    rng = np.random.default_rng(seed % 1000)
+    lens = rng.integers(0, 200, size=6)
+    for s, L in enumerate(lens):
+        prod.pa_alloc_add_seq(s, int(L))
+        ref.add_seq(s, int(L))
+    ids = np.arange(6)
+    for _ in range(40):
+        a = prod.pa_alloc_append_batch(ids)
+        b = np.array([ref.append(int(s)) for s in ids], np.int32)
+        assert np.array_equal(a, b)
+    assert np.array_equal(prod.pa_alloc_block_tables(ids, 20), ref.block_tables(ids, 20))
+    assert np.array_equal(prod.pa_alloc_context_lens(ids), ref.context_lens(ids))
+    for s, L in enumerate(lens):
+        assert np.array_equal(prod.pa_alloc_slots(s, 0, int(L)), ref.slots(s, 0, int(L)))
+    prod.pa_alloc_free_seq(3)
+    ref.free_seq(3)
+    prod.pa_alloc_add_seq(9, 40)
+    ref.add_seq(9, 40)
+    assert np.array_equal(prod.pa_alloc_block_tables([9], 5), ref.block_tables([9], 5))
+    assert prod.num_free == ref.num_free
+
+
+def test_allocator_errors_and_all_or_nothing_batch(pa):
+    prod = pa.PagedAllocator(3, 8, 7)
+    prod.pa_alloc_add_seq(0, 8)
+    prod.pa_alloc_add_seq(1, 8)
+    prod.pa_alloc_add_seq(2, 1)
+    with pytest.raises(pa.PANoBlocks):
+        prod.pa_alloc_append_batch([0, 1])          # needs 2 new blocks, 0 free
+    assert list(prod.pa_alloc_context_lens([0, 1, 2])) == [8, 8, 1]
+    with pytest.raises(pa.PAError):
+        prod.pa_alloc_append_batch([2, 2])          # duplicate id
+    with pytest.raises(pa.PAError):
+        prod.pa_alloc_add_seq(0, 1)                 # already live
+    with pytest.raises(pa.PAError):
+        prod.pa_alloc_append(42)                    # unknown id
+    slots = prod.pa_alloc_append_batch([2])
+    assert slots.shape == (1,) and slots[0] % 8 == 1
