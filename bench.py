@@ -424,6 +424,29 @@ def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
                     "pa_decode_step, D2H of out, stream sync; wall clock"}
 
 
+def run_profile_case(args):
+    """Small, self-contained case for ncu: decode steps of one workload only."""
+    import torch
+    import paged_kv_cache_187_gb300 as pa
+    from paged_kv_cache_187_gb300 import workloads as W
+    from paged_kv_cache_187_gb300.runner import DecodeRunner
+    w = W.WORKLOADS[args.profile_workload]
+    r = DecodeRunner(w, device="cuda").next_step()
+    r.run_reshape()
+    del r.k_prefill, r.v_prefill          # not needed for decoding: keep the footprint small
+    torch.cuda.empty_cache()
+    if args.gqa_cuda_cores:
+        pa.pa_set_gqa_tensor_cores(False)
+    variant = args.variant
+    for _ in range(args.warmup + args.steps):
+        r.run_decode(variant, partition_size=args.partition_size)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    print(json.dumps({"profile_case": w.name, "variant": variant, "steps": args.steps,
+                      "warmup": args.warmup, "gqa_cuda_cores": bool(args.gqa_cuda_cores),
+                      "bytes_per_decode": r.kv_bytes()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,7 +456,16 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-workload", default=None,
+                    help="run only decode steps of this workload (a small case for ncu)")
+    ap.add_argument("--variant", default="auto", choices=["auto", "v1", "v2"])
+    ap.add_argument("--partition-size", type=int, default=None)
+    ap.add_argument("--gqa-cuda-cores", action="store_true",
+                    help="profile case: force the CUDA-core path for grouped-query heads")
     args = ap.parse_args()
+    if args.profile_workload:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
