@@ -178,6 +178,37 @@ pa_status pa_decode_step(void* out, const void* query, const void* key, const vo
  * Process-wide; both paths meet the same tolerance. */
 pa_status pa_set_gqa_tensor_cores(int32_t enable);
 
+/* ------------------------------------------------------------------------------ */
+/* V2 decode for callers that cannot allocate device memory                         */
+/* ------------------------------------------------------------------------------ */
+/* The paper has no counterpart to this call; it exists for callers that are not
+ * allowed to allocate device memory and have no workspace handed to them -- for
+ * example a plugin's enqueue path inside an inference runtime that owns all device
+ * memory, or code that must not call cudaMalloc while a stream is being captured.
+ *
+ * pa_decode_v2_noalloc computes exactly what pa_decode_v2 computes, but its scratch
+ * (work counter, partition list, partial results) lives in one static device array of
+ * PA_NOALLOC_SCRATCH_BYTES compiled into the library.  Every GPU that loads the library
+ * keeps that array until the process exits.  The caller still passes inputs and outputs.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - If pa_decode_v2_workspace_size() for the arguments exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES, it returns PA_ERR_WORKSPACE and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture begins.
+ *   - All calls share the one array and it keeps the last call's contents (each call
+ *     rewrites everything it reads).  Calls whose kernels overlap on the GPU -- on two
+ *     streams, or from two threads -- race on it and give wrong results; serialise them. */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+pa_status pa_decode_v2_noalloc(void* out, const void* query, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_size, int32_t block_size, int32_t num_blocks,
+                               int32_t max_context_len, float scale, pa_dtype dtype,
+                               int32_t partition_size, int32_t* status_dev, pa_stream stream);
+
 /* Profiling hook: when both are non-NULL (cudaEvent_t handles), every later decode
  * call records `start_event` on its stream right before it launches the paged decode
  * kernel and `stop_event` right after, so that the kernel alone can be timed with

@@ -63,6 +63,8 @@ def _load():
         "pa_decode_v2_workspace_size": ([i32, i32, i32, i32, i32], sz),
         "pa_decode_v2": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32,
                           P, sz, P, P], i32),
+        "pa_decode_v2_noalloc": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                  i32, i32, P, P], i32),
         "pa_decode_auto_plan": ([i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                  ctypes.POINTER(i32)], i32),
         "pa_decode_auto_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
@@ -210,6 +212,22 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, context_lens,
     _check(_lib.pa_decode_v2(*ptrs, S, Hq, Hkv, D, bs, NB, int(max_context_len), float(scale), dt,
                              int(partition_size), wp, wb, _opt_dev(status, "status"),
                              _stream(stream)))
+
+
+PA_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def pa_decode_v2_noalloc(out, query, key_cache, value_cache, block_tables, context_lens,
+                         max_context_len: int, scale: float, partition_size: int, status=None,
+                         stream=None):
+    """pa_decode_v2 without a workspace argument: the library's fixed device scratch is
+    used instead, and nothing is allocated.  For callers that may not allocate device
+    memory; calls that overlap on the GPU share that scratch and must be serialised."""
+    ptrs, (S, Hq, Hkv, D, bs, NB), dt = _decode_common(out, query, key_cache, value_cache,
+                                                       block_tables, context_lens)
+    _check(_lib.pa_decode_v2_noalloc(*ptrs, S, Hq, Hkv, D, bs, NB, int(max_context_len),
+                                     float(scale), dt, int(partition_size),
+                                     _opt_dev(status, "status"), _stream(stream)))
 
 
 def pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,

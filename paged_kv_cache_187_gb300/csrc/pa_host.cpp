@@ -324,6 +324,11 @@ void auto_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t block_size,
 
 namespace pa {
 
+int32_t set_last_error(int32_t status, const char* message) {
+    g_last_error = message ? message : "";
+    return status;
+}
+
 WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                     int32_t max_context_len, int32_t partition_size) {
     WorkspaceLayout L;

@@ -69,6 +69,9 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                                      int32_t head_size, int32_t block_size, int32_t num_blocks,
                                      int32_t* status, cudaStream_t stream);
 
+// Records `message` as this thread's pa_last_error() text and returns `status`.
+int32_t set_last_error(int32_t status, const char* message);
+
 // Resident CTAs per SM of a decode instantiation (0 if it cannot launch).
 int32_t decode_ctas_per_sm(const KernelKey& key);
 
