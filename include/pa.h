@@ -139,9 +139,12 @@ pa_status pa_decode_v2(void* out, const void* query, const void* key_cache,
                        int32_t* status_dev, pa_stream stream);
 
 /* Which variant pa_decode_auto runs for these host-known sizes.
- * *variant = 1 (V1) or 2 (V2); *partition_size = the V2 partition size (0 for V1).
- * The choice follows [TALK]: whole sequences per unit while there are enough units to
- * fill every SM several times over and no context is long; partitions otherwise. */
+ * *variant = 1 (V1) or 2 (V2); for V2, *partition_size is the smallest partition the
+ * call may use (0 for V1).  The choice follows [TALK]: whole sequences per unit while
+ * every context is short and there are units to fill every SM several times over;
+ * otherwise V2 with partitions sized on the device from the actual context lengths --
+ * as large as still gives every persistent CTA several units, so that few sequences
+ * need a merge -- handed out longest first. */
 pa_status pa_decode_auto_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                               int32_t head_size, int32_t block_size, int32_t max_context_len,
                               int32_t* variant, int32_t* partition_size);

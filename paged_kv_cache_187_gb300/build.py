@@ -43,19 +43,26 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths if os.path.exists(p))
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile (if stale) and return the path of libpa.so."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          defines: tuple = (), out: str | None = None) -> str:
+    """Compile (if stale) and return the path of libpa.so.
+
+    ``defines`` (e.g. ``("PA_CORE_CONSUMERS=4",)``) and ``out`` build a variant of the
+    library elsewhere for tuning sweeps; the default build ignores both."""
+    lib = out or LIB
+    build_dir = BUILD if not defines else os.path.join(BUILD, "variant_" + "_".join(defines))
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", os.path.join(ROOT, "include"), "-I", CSRC]
+    common += ["-D" + d for d in defines]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0 or verbose or ptxas_info:
@@ -66,14 +73,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link of libpa.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -2,9 +2,9 @@
 //   * reshape_and_cache: scatters each step's new K/V rows into the paged pools through
 //     slot_mapping ("[core] Multi Step Scheduling #7000", the slot_mapping / block_tables
 //     metadata a decode step carries);
-//   * plan: lists the V2 partitions of every sequence and resets the work counter;
-//   * reduce: merges the partitions of a sequence by log-sum-exp ("vLLM Project Update"
-//     talk, the V2 kernel "similar to flash decoding").
+//   * plan: lists the V2 partitions of every sequence ("vLLM Project Update" talk, the V2
+//     kernel that partitions sequences and spreads them over SMs) in claim order and
+//     resets the counters the decode kernel uses.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(128)
                              const int32_t* __restrict__ slot_mapping, int32_t num_kv_heads,
                              int32_t head_size, int32_t block_size, int32_t num_blocks,
                              int32_t* status) {
+    allow_dependent_launch();   // the decode kernel may set up meanwhile (it waits for us)
     const int32_t i = blockIdx.x;
     const int64_t slot = slot_mapping[i];
     if (slot < 0) return;                                   // padding token
@@ -57,99 +58,152 @@ __global__ void __launch_bounds__(128)
     }
 }
 
-// Single CTA: per-sequence partition counts, exclusive scan, the (sequence, partition)
-// list, and the work counter reset.
-__global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
-    __shared__ int32_t warp_sums[32];
-    __shared__ int32_t carry_s;
-    const int32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int32_t P = p.partition_size;
-    if (tid == 0) carry_s = 0;
+// Block-wide exclusive scan of x over blockDim.x (a multiple of 32) threads; *total
+// receives the sum.  `buf` holds 32 ints of shared memory.
+__device__ __forceinline__ int32_t block_excl_scan(int32_t x, int32_t* buf, int32_t* total) {
+    const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int32_t v = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane == 31) buf[warp] = v;
     __syncthreads();
-    for (int32_t base = 0; base < p.num_seqs; base += 1024) {
-        const int32_t s = base + tid;
-        int32_t np = 0;
-        if (s < p.num_seqs) {
-            const int32_t L = clamp_len(p, s, true);
-            np = L > 0 ? (L + P - 1) / P : 1;      // an empty context is one empty unit
-        }
-        // block-wide exclusive scan of np
-        int32_t x = np;
+    if (warp == 0) {
+        int32_t w = lane < nw ? buf[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
         }
-        if (lane == 31) warp_sums[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int32_t w = warp_sums[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o) w += y;
-            }
-            warp_sums[lane] = w;                   // inclusive over warps
-        }
-        __syncthreads();
-        const int32_t carry = carry_s;
-        const int32_t excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - np;
-        if (s < p.num_seqs) {
-            p.part_offset[s] = excl;
-            for (int32_t j = 0; j < np; ++j) p.part_list[excl + j] = make_int2(s, j);
-        }
-        __syncthreads();
-        if (tid == 0) carry_s = carry + warp_sums[31];
-        __syncthreads();
+        buf[lane] = w;                       // inclusive over warps
     }
-    if (tid == 0) {
-        const int32_t total = carry_s;
-        p.part_offset[p.num_seqs] = total;
-        p.hdr->total_parts = (uint32_t)total;
-        p.hdr->total_units = (uint32_t)total * (uint32_t)p.num_kv_heads;
-        p.hdr->counter = 0;
-    }
+    __syncthreads();
+    const int32_t excl = (warp > 0 ? buf[warp - 1] : 0) + v - x;
+    *total = buf[31];
+    __syncthreads();
+    return excl;
 }
 
-// One CTA per (sequence, kv head) with more than one partition; a thread per
-// (query head of the group, 4 head dims).  Partials hold unnormalised sums acc_p,
-// the running max m_p (base-2 units) and the exp-sum l_p:
-//   out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,   M = max_p m_p.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(128) reduce_kernel(const DecodeParams p) {
-    const int32_t s = blockIdx.x, kvh = blockIdx.y;
-    const int32_t L = clamp_len(p, s, false);
-    if (L <= p.partition_size) return;                      // written by the decode kernel
-    const int32_t np = (L + p.partition_size - 1) / p.partition_size;
-    const int32_t base = p.part_offset[s];
-    const int32_t g = p.group;
-    for (int32_t idx = threadIdx.x; idx < g * (D / 4); idx += blockDim.x) {
-        const int32_t h = kvh * g + idx / (D / 4);
-        const int32_t d = (idx % (D / 4)) * 4;
-        float M = -INFINITY;
-        for (int32_t j = 0; j < np; ++j)
-            M = fmaxf(M, p.part_ml[(size_t)(base + j) * p.num_q_heads + h].x);
-        float den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int32_t j = 0; j < np; ++j) {
-            const float2 ml = p.part_ml[(size_t)(base + j) * p.num_q_heads + h];
-            float w;
-            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(w) : "f"(ml.x - M));
-            den += w * ml.y;
-            const float4 a = *reinterpret_cast<const float4*>(
-                p.part_acc + ((size_t)(base + j) * p.num_q_heads + h) * D + d);
-            acc.x += w * a.x;
-            acc.y += w * a.y;
-            acc.z += w * a.z;
-            acc.w += w * a.w;
+constexpr int kTailBuckets = 256;
+
+// Adaptive partitioning aims at this many work units per persistent CTA: enough for the
+// longest-first order to even out the CTAs' finishing times, few enough that most
+// sequences need no merge at all.
+#ifndef PA_UNITS_PER_CTA
+#define PA_UNITS_PER_CTA 2
+#endif
+
+// Single CTA.  Lists the V2 partitions of every sequence in the order the persistent
+// decode CTAs will claim them -- all full partitions first, then the partial ones from
+// the longest to the shortest, so that the last units handed out are the cheapest
+// (longest-processing-time-first) -- and resets the work counter and the per
+// (sequence, kv head) arrival counters.  Entry: (sequence, partition, first partition
+// slot of the sequence, clamped context length).  Partition slots (where partial
+// results go) are numbered sequence by sequence, independent of the claim order.
+__global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
+    __shared__ int32_t scan_buf[32];
+    __shared__ int32_t hist[kTailBuckets];    // tail partitions per size bucket
+    __shared__ int32_t bstart[kTailBuckets];
+    __shared__ unsigned long long total_tokens;
+    __shared__ int32_t P_s;
+    allow_dependent_launch();   // the decode kernel may set up meanwhile (it waits for us)
+    const int32_t tid = threadIdx.x;
+    const int32_t bs = p.block_size;
+    for (int32_t i = tid; i < kTailBuckets; i += blockDim.x) hist[i] = 0;
+    if (tid == 0) total_tokens = 0ull;
+    __syncthreads();
+    // pass 0: the partition size.  Fixed (pa_decode_v2), or adaptive: the largest
+    // multiple of block_size, not below the given minimum, that still yields about
+    // PA_UNITS_PER_CTA units per CTA.
+    if (p.adaptive) {
+        unsigned long long mine = 0;
+        for (int32_t s = tid; s < p.num_seqs; s += blockDim.x) mine += (unsigned)clamp_len(p, s, false);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        if ((tid & 31) == 0) atomicAdd(&total_tokens, mine);   // one shared atomic per warp
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned long long work = total_tokens * (unsigned long long)p.num_kv_heads;
+            const unsigned long long want = (unsigned long long)max(p.grid_ctas, 1) * PA_UNITS_PER_CTA;
+            unsigned long long Pa = (work / want / (unsigned)bs) * (unsigned)bs;
+            if (Pa > (1ull << 30)) Pa = 1ull << 30;
+            P_s = max(p.partition_size, (int32_t)Pa);
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        uint2 o;
-        o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
-        o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) +
-                                  ((size_t)s * p.num_q_heads + h) * D + d) = o;
+    } else if (tid == 0) {
+        P_s = p.partition_size;
     }
+    __syncthreads();
+    const int32_t P = P_s;
+    // pass 1: counts
+    int32_t parts = 0, full_parts = 0;
+    for (int32_t base = 0; base < p.num_seqs; base += blockDim.x) {
+        const int32_t s = base + tid;
+        int32_t np = 0, nf = 0;
+        if (s < p.num_seqs) {
+            const int32_t L = clamp_len(p, s, true);
+            nf = L / P;
+            const int32_t tail = L - nf * P;
+            np = nf + ((tail > 0 || L == 0) ? 1 : 0);
+            if (tail > 0 || L == 0) {
+                const int32_t b = min((tail + bs - 1) / bs, kTailBuckets - 1);
+                atomicAdd(&hist[b], 1);
+            }
+        }
+        int32_t tp, tf;
+        block_excl_scan(np, scan_buf, &tp);
+        block_excl_scan(nf, scan_buf, &tf);
+        parts += tp;
+        full_parts += tf;
+    }
+    __syncthreads();
+    {   // first list position of each tail bucket: longer tails first
+        const int32_t b = kTailBuckets - 1 - tid;
+        int32_t tb;
+        const int32_t ex = block_excl_scan(tid < kTailBuckets ? hist[b] : 0, scan_buf, &tb);
+        if (tid < kTailBuckets) bstart[b] = full_parts + ex;
+        __syncthreads();
+        if (tid < kTailBuckets) hist[tid] = 0;              // reused as fill counters
+        __syncthreads();
+    }
+    // pass 2: positions
+    int32_t carry_np = 0, carry_nf = 0;
+    for (int32_t base = 0; base < p.num_seqs; base += blockDim.x) {
+        const int32_t s = base + tid;
+        int32_t np = 0, nf = 0, L = 0, tail = 0;
+        if (s < p.num_seqs) {
+            L = clamp_len(p, s, false);
+            nf = L / P;
+            tail = L - nf * P;
+            np = nf + ((tail > 0 || L == 0) ? 1 : 0);
+        }
+        int32_t tp, tf;
+        const int32_t slot0 = carry_np + block_excl_scan(np, scan_buf, &tp);
+        const int32_t full0 = carry_nf + block_excl_scan(nf, scan_buf, &tf);
+        if (s < p.num_seqs) {
+            for (int32_t j = 0; j < nf; ++j) p.part_list[full0 + j] = make_int4(s, j, slot0, L);
+            if (tail > 0 || L == 0) {
+                const int32_t b = min((tail + bs - 1) / bs, kTailBuckets - 1);
+                const int32_t pos = bstart[b] + atomicAdd(&hist[b], 1);
+                p.part_list[pos] = make_int4(s, nf, slot0, L);
+            }
+        }
+        carry_np += tp;
+        carry_nf += tf;
+    }
+    const int32_t pairs = p.num_seqs * p.num_kv_heads;
+    for (int32_t i = tid; i < pairs; i += blockDim.x) p.arrive[i] = 0;
+    if (tid == 0) {
+        p.hdr->total_parts = (uint32_t)parts;
+        p.hdr->total_units = (uint32_t)parts * (uint32_t)p.num_kv_heads;
+        p.hdr->partition_size = (uint32_t)P;
+        p.hdr->counter = 0;
+    }
+    // This kernel may run alongside the reshape_and_cache launch before it (it reads
+    // nothing that launch writes).  Finish only after that launch has, so that the
+    // decode kernel, which waits for this one, also sees the new K/V rows.
+    grid_dependency_wait();
 }
 
 }  // namespace
@@ -168,22 +222,20 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
 }
 
 cudaError_t launch_plan(const DecodeParams& p, cudaStream_t stream) {
-    plan_kernel<<<1, 1024, 0, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_reduce(const DecodeParams& p, int32_t head_size, bool bf16,
-                          cudaStream_t stream) {
-    dim3 grid(p.num_seqs, p.num_kv_heads);
-    if (p.num_seqs <= 0) return cudaSuccess;
-    if (head_size == 128) {
-        if (bf16) reduce_kernel<128, true><<<grid, 128, 0, stream>>>(p);
-        else reduce_kernel<128, false><<<grid, 128, 0, stream>>>(p);
-    } else {
-        if (bf16) reduce_kernel<64, true><<<grid, 128, 0, stream>>>(p);
-        else reduce_kernel<64, false><<<grid, 128, 0, stream>>>(p);
-    }
-    return cudaGetLastError();
+    // Programmatic dependent launch: may start while a preceding reshape_and_cache runs.
+    // A preceding decode kernel never lets it start early, so the workspace it rewrites
+    // is no longer in use when it does.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, p);
 }
 
 }  // namespace pa

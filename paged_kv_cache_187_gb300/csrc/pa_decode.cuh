@@ -6,20 +6,24 @@
 //     out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) v_t,   t < context_len[s],
 // where token t lives in row t % block_size of physical block block_tables[s][t / bs],
 // kv head h / group.  A work unit is (sequence, kv head, token range): the whole
-// context (V1) or one partition of partition_size tokens (V2), whose partial
-// (max, exp-sum, unnormalised sum) is merged afterwards by log-sum-exp.
+// context (V1) or one partition of partition_size tokens (V2).  A V2 unit of a sequence
+// with several partitions stores its partial (max, exp-sum, unnormalised sum); the last
+// unit of that (sequence, kv head) to finish merges all partials by log-sum-exp, so no
+// separate reduction launch is needed.
 //
-// GB300 design (one CTA = 2 warps, several CTAs per SM):
-//   * warp 0 (producer) claims work units, copies the unit's query rows with a 1-D bulk
-//     copy, and streams the unit's K and V tiles -- one (block, kv head) tile is
-//     block_size x head_size contiguous elements -- with 2-D tensor TMA into an
-//     NSTAGE-deep ring of shared-memory stages (128-byte swizzle, L2 evict-first).
-//   * warp 1 (consumer) runs the online softmax over the tiles as they land:
+// GB300 design (one CTA = 1 producer warp + NCONS consumer warps, several CTAs per SM):
+//   * the producer claims work units, copies the unit's query rows with a 1-D bulk copy,
+//     and streams the unit's K and V tiles -- one (block, kv head) tile is block_size x
+//     head_size contiguous elements -- with 2-D tensor TMA into an NSTAGE-deep ring of
+//     shared-memory stages (128-byte swizzle, L2 evict-first);
+//   * consumer c takes tiles c, c + NCONS, ... of each unit and runs the online softmax
+//     over them; the consumers' states are merged through shared memory at the end of
+//     the unit:
 //       - group >= 2 (GQA): S^T = K_tile Q^T and O^T += V_tile^T P^T on the tensor cores
 //         (mma.sync m16n8k16, tokens / head dims on M, the group's query heads on N),
 //         P moved from accumulator to operand layout with movmatrix;
 //       - group 1 (MHA) or on request: CUDA cores, each lane owning head_size/32 dims,
-//         dot products finished by a transposed butterfly reduction.
+//         dot products finished by a transposed butterfly reduction;
 //   * all barrier waits are bounded; a timeout is reported, never hung on.
 #pragma once
 
@@ -37,10 +41,20 @@ namespace pa {
 #define PA_DEVERR_BAD_LEN_ 4
 #define PA_DEVERR_TIMEOUT_ 8
 
+// Tiles of the current unit still to issue when the producer claims the next unit.
+#ifndef PA_CLAIM_LEAD
+#define PA_CLAIM_LEAD 8
+#endif
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^(m - M) with the convention that an empty state (m = -inf) weighs 0.
+__device__ __forceinline__ float state_weight(float m, float M) {
+    return m == -INFINITY ? 0.f : fast_exp2(m - M);
 }
 
 __device__ __forceinline__ void flag_error(int32_t* status, int32_t bit) {
@@ -60,16 +74,42 @@ __device__ __forceinline__ int32_t clamped_len(const DecodeParams& p, int32_t s,
     return L;
 }
 
+// Named barrier 1 among the consumer warps only (the producer never joins it) that
+// also ORs a flag over every consumer thread, so all consumers take the same branch.
+__device__ __forceinline__ bool consumers_any(bool v, int nthreads) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// A bounded barrier wait whose result is the same in every lane of the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Is the CTA aborting?  The same answer in every lane of the warp.
+__device__ __forceinline__ bool warp_sees_abort(const volatile int32_t& flag) {
+    return __any_sync(0xffffffffu, flag != 0);
+}
+
 struct UnitDesc {
     int32_t seq;     // -1: no more units
     int32_t kvh;
     int32_t tok0;    // first token of the unit (a multiple of block_size)
     int32_t tok1;    // one past the last token
     int32_t pslot;   // partition slot for partial results, -1: write the final output
-    int32_t pad[3];
+    int32_t pbase;   // first partition slot of the sequence
+    int32_t nparts;  // partitions of the sequence
+    int32_t pad;
 };
 
-template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_>
+template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_, int NCONS_>
 struct DecodeCfg {
     static constexpr int D = D_;
     static constexpr int BS = BS_;
@@ -79,41 +119,150 @@ struct DecodeCfg {
     static constexpr int NT = MMA_ ? HCAP_ / 8 : 0;  // mma n-tiles of 8 heads
     static constexpr int NSTAGE = NSTAGE_;
     static constexpr int NQ = NQ_;
+    static constexpr int NCONS = NCONS_;           // consumer warps per CTA
     static constexpr int HALVES = D / 64;          // 128-byte swizzle spans 64 elements
     static constexpr int TILE_BYTES = D * BS * 2;  // one (block, kv head) tile of K or V
     static constexpr int HALF_BYTES = BS * 128;
     static constexpr int QROWS = HCAP;
-    static constexpr int THREADS = 64;
+    static constexpr int THREADS = 32 * (1 + NCONS);
+    // per-lane floats of one consumer's softmax state (m, l, acc)
+    static constexpr int NSTATE = MMA_ ? (4 * NT + (D / 16) * NT * 4) : (2 * HCAP_ + HCAP_ * (D / 32));
     static_assert(D == 64 || D == 128, "head_size");
     static_assert(BS == 16 || BS == 32, "block_size");
     static_assert(!MMA_ || HCAP_ == 8 || HCAP_ == 16, "mma heads");
     static_assert(MMA_ || HCAP_ == 1 || HCAP_ == 2 || HCAP_ == 4 || HCAP_ == 8, "heads");
+    static_assert(NCONS >= 1 && NCONS <= 4, "consumers");
+    // Consumer c takes tiles c, c + NCONS, ... of a unit, and tile k lands in stage
+    // k % NSTAGE.  With NSTAGE a multiple of NCONS, the previous use of a stage (tile
+    // k - NSTAGE) belongs to the same consumer, so a consumer never waits on a stage that
+    // is two phases behind -- where the mbarrier parity test would pass too early.
+    static_assert(NSTAGE % NCONS == 0, "stages must be a multiple of the consumer warps");
 };
 
 template <class C>
 struct alignas(1024) DecodeSmem {
     uint8_t kv[C::NSTAGE][2][C::TILE_BYTES];         // stage: K tile then V tile
     alignas(128) uint8_t qbuf[C::NQ][C::QROWS * C::D * 2];
-    alignas(128) float ostage[C::QROWS * C::D];      // output staging (consumer)
-    float pbuf[C::QROWS][8];                         // CUDA-core path: softmax weights
+    alignas(128) float ostage[C::QROWS * C::D];      // output staging (consumer 0)
+    float xbuf[C::NCONS > 1 ? C::NCONS - 1 : 1][C::NSTATE * 32];  // consumer states to merge
+    alignas(16) float pbuf[C::NCONS][C::QROWS][C::BS];   // CUDA-core path: softmax weights
     uint64_t full[C::NSTAGE];
     uint64_t empty[C::NSTAGE];
     uint64_t qfull[C::NQ];
     uint64_t qempty[C::NQ];
     UnitDesc unit[C::NQ];
     uint32_t issued[C::NSTAGE];    // tiles issued into each stage (producer)
-    uint32_t consumed[C::NSTAGE];  // tiles consumed from each stage (consumer)
+    uint32_t consumed[C::NSTAGE];  // tiles consumed from each stage (consumers)
     uint32_t qissued[C::NQ];
     uint32_t qconsumed[C::NQ];
     volatile int32_t abort;
 };
 
-// Byte offset of element pair / chunk inside a swizzled tile: row t, 16-byte chunk c16
-// of the head_size-element row.  The tile is stored as [D/64][BS][128 B], each 128-byte
-// line with its 16-byte chunks permuted by (line index % 8), the TMA 128B swizzle.
+// Byte offset of 16-byte chunk c16 of row t inside a swizzled tile.  The tile is stored
+// as [D/64][BS][128 B], each 128-byte line with its 16-byte chunks permuted by
+// (line index % 8): the TMA 128B swizzle.
 template <class C>
 __device__ __forceinline__ uint32_t swz(int t, int c16) {
     return (uint32_t)((c16 >> 3) * C::HALF_BYTES + t * 128 + ((((c16 & 7) ^ (t & 7))) << 4));
+}
+
+// ---------------------------------------------------------------------------------
+// Output / partial writers shared by both consumer types.
+// ---------------------------------------------------------------------------------
+template <class C>
+__device__ __forceinline__ void store_row16(const DecodeParams& p, int32_t seq, int32_t head,
+                                            int d0, const float (&v)[4]) {
+    uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + ((size_t)seq * p.num_q_heads + head) * C::D + d0;
+    uint2 w;
+    w.x = pack2<C::kBf16>(v[0], v[1]);
+    w.y = pack2<C::kBf16>(v[2], v[3]);
+    *reinterpret_cast<uint2*>(o) = w;
+}
+
+// The last finished unit of a (sequence, kv head) merges every partition's partial:
+//   out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p,
+// as one online pass over the partitions, four at a time so that each lane has 4 x NI
+// independent L2 loads in flight.  Lane handles (head, 4 dims) chunks lane, lane + 32,
+// ...  Partials were written by other CTAs: read them through L2 (ld.global.cg).
+template <class C>
+__device__ __forceinline__ void merge_partitions(const DecodeParams& p, const UnitDesc& u, int lane) {
+    constexpr int CPH = C::D / 4;                         // 4-dim chunks per head
+    constexpr int NI = (C::HCAP * CPH + 31) / 32;         // chunks per lane, at most
+    const int g = p.group;
+    const int np = u.nparts;
+    float M[NI], den[NI], a[NI][4];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        M[i] = -INFINITY;
+        den[i] = 0.f;
+        a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0.f;
+    }
+    for (int j0 = 0; j0 < np; j0 += 4) {
+        float2 ml[4][NI];
+        float4 x[4][NI];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const int idx = lane + 32 * i;
+                const int j = j0 + jj;
+                ml[jj][i] = make_float2(-INFINITY, 0.f);
+                x[jj][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < np && idx < g * CPH) {
+                    const size_t row = (size_t)(u.pbase + j) * p.num_q_heads + u.kvh * g + idx / CPH;
+                    ml[jj][i] = __ldcg(&p.part_ml[row]);
+                    x[jj][i] = __ldcg(reinterpret_cast<const float4*>(p.part_acc + row * C::D) + idx % CPH);
+                }
+            }
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            float Mn = M[i];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) Mn = fmaxf(Mn, ml[jj][i].x);
+            const float f = state_weight(M[i], Mn);
+            den[i] *= f;
+            a[i][0] *= f;
+            a[i][1] *= f;
+            a[i][2] *= f;
+            a[i][3] *= f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float w = state_weight(ml[jj][i].x, Mn);
+                den[i] += w * ml[jj][i].y;
+                a[i][0] += w * x[jj][i].x;
+                a[i][1] += w * x[jj][i].y;
+                a[i][2] += w * x[jj][i].z;
+                a[i][3] += w * x[jj][i].w;
+            }
+            M[i] = Mn;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const int idx = lane + 32 * i;
+        if (idx < g * CPH) {
+            const float inv = den[i] > 0.f ? 1.f / den[i] : 0.f;
+            float v[4] = {a[i][0] * inv, a[i][1] * inv, a[i][2] * inv, a[i][3] * inv};
+            store_row16<C>(p, u.seq, u.kvh * g + idx / CPH, (idx % CPH) * 4, v);
+        }
+    }
+}
+
+// After this unit's partial is stored: count it, and merge if it was the last one.
+template <class C>
+__device__ __forceinline__ void finish_partition(const DecodeParams& p, const UnitDesc& u, int lane) {
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        const int t = atomicAdd(&p.arrive[(size_t)u.seq * p.num_kv_heads + u.kvh], 1);
+        last = (t == u.nparts - 1);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __threadfence();
+        merge_partitions<C>(p, u, lane);
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -160,7 +309,7 @@ struct MmaConsumer {
 
     // One tile of BS tokens, `valid` (1..BS) of which belong to the unit.
     __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid,
-                                         float scale_log2, int lane) {
+                                         float scale_log2, int lane, float (*)[BS]) {
         const int r8 = lane & 7, mi = lane >> 3;
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
         // S^T[token][head] = K Q^T
@@ -259,6 +408,49 @@ struct MmaConsumer {
         }
     }
 
+    __device__ __forceinline__ void export_state(float* buf, int lane) const {
+        int k = 0;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                buf[(k++) * 32 + lane] = m[nt][j];
+                buf[(k++) * 32 + lane] = l[nt][j];
+            }
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) buf[(k++) * 32 + lane] = acc[i][nt][r];
+    }
+
+    __device__ __forceinline__ void merge_state(const float* buf, int lane) {
+        float a[NT][2], b[NT][2];
+        int k = 0;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float mo = buf[(k++) * 32 + lane];
+                const float lo = buf[(k++) * 32 + lane];
+                const float M = fmaxf(m[nt][j], mo);
+                a[nt][j] = state_weight(m[nt][j], M);
+                b[nt][j] = state_weight(mo, M);
+                m[nt][j] = M;
+                l[nt][j] = a[nt][j] * l[nt][j] + b[nt][j] * lo;
+            }
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float o = buf[(k++) * 32 + lane];
+                    acc[i][nt][r] = a[nt][r & 1] * acc[i][nt][r] + b[nt][r & 1] * o;
+                }
+    }
+
     // Writes the unit's result: final rows of `out` (pslot < 0) or a partial.
     __device__ __forceinline__ void finish(float* ostage, const DecodeParams& p, const UnitDesc& u,
                                            int lane) {
@@ -274,7 +466,7 @@ struct MmaConsumer {
                 lt[nt][j] = v;
             }
         const bool final_out = u.pslot < 0;
-        // stage [head][dim] in fp32
+        // stage [head][dim] in fp32 so the rows leave as contiguous vectors
 #pragma unroll
         for (int i = 0; i < KS; ++i)
 #pragma unroll
@@ -291,8 +483,24 @@ struct MmaConsumer {
                     ostage[h * D + d] = v;
                 }
         __syncwarp();
-        write_rows<C>(ostage, p, u, lane, final_out);
-        if (!final_out) {
+        const int g = p.group;
+        if (final_out) {
+            uint16_t* out = reinterpret_cast<uint16_t*>(p.out) +
+                            ((size_t)u.seq * p.num_q_heads + (size_t)u.kvh * g) * D;
+            for (int c = lane; c < g * D / 8; c += 32) {
+                const float* src = ostage + c * 8;
+                uint4 w;
+                w.x = pack2<C::kBf16>(src[0], src[1]);
+                w.y = pack2<C::kBf16>(src[2], src[3]);
+                w.z = pack2<C::kBf16>(src[4], src[5]);
+                w.w = pack2<C::kBf16>(src[6], src[7]);
+                *reinterpret_cast<uint4*>(out + (size_t)c * 8) = w;
+            }
+        } else {
+            float* dst = p.part_acc + ((size_t)u.pslot * p.num_q_heads + (size_t)u.kvh * g) * D;
+            for (int c = lane; c < g * D / 4; c += 32)
+                *reinterpret_cast<float4*>(dst + (size_t)c * 4) =
+                    *reinterpret_cast<const float4*>(ostage + c * 4);
             // (m, l) per head: lanes 0..3 hold heads 2*lane, 2*lane+1 of each n-tile
             if (lane < 4) {
 #pragma unroll
@@ -300,40 +508,14 @@ struct MmaConsumer {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int h = nt * 8 + 2 * lane + j;
-                        if (h < p.group)
-                            p.part_ml[(size_t)u.pslot * p.num_q_heads + u.kvh * p.group + h] =
+                        if (h < g)
+                            p.part_ml[(size_t)u.pslot * p.num_q_heads + u.kvh * g + h] =
                                 make_float2(m[nt][j], lt[nt][j]);
                     }
             }
+            finish_partition<C>(p, u, lane);
         }
         __syncwarp();
-    }
-
-    template <class CC>
-    static __device__ __forceinline__ void write_rows(const float* ostage, const DecodeParams& p,
-                                                      const UnitDesc& u, int lane, bool final_out) {
-        const int g = p.group;
-        if (final_out) {
-            // 16-bit rows, 8 elements (16 bytes) per lane per step
-            uint16_t* out = reinterpret_cast<uint16_t*>(p.out) +
-                            ((size_t)u.seq * p.num_q_heads + (size_t)u.kvh * g) * CC::D;
-            const int chunks = g * CC::D / 8;
-            for (int c = lane; c < chunks; c += 32) {
-                const float* src = ostage + c * 8;
-                uint4 w;
-                w.x = pack2<CC::kBf16>(src[0], src[1]);
-                w.y = pack2<CC::kBf16>(src[2], src[3]);
-                w.z = pack2<CC::kBf16>(src[4], src[5]);
-                w.w = pack2<CC::kBf16>(src[6], src[7]);
-                *reinterpret_cast<uint4*>(out + (size_t)c * 8) = w;
-            }
-        } else {
-            float* dst = p.part_acc + ((size_t)u.pslot * p.num_q_heads + (size_t)u.kvh * g) * CC::D;
-            const int chunks = g * CC::D / 4;
-            for (int c = lane; c < chunks; c += 32)
-                *reinterpret_cast<float4*>(dst + (size_t)c * 4) =
-                    *reinterpret_cast<const float4*>(ostage + c * 4);
-        }
     }
 };
 
@@ -342,11 +524,10 @@ struct MmaConsumer {
 // ---------------------------------------------------------------------------------
 template <class C>
 struct CoreConsumer {
-    static constexpr int D = C::D, BS = C::BS, G = C::HCAP, DPL = D / 32;
+    static constexpr int D = C::D, BS = C::BS, G = C::HCAP, DPL = D / 32, NC8 = BS / 8;
     float qf[G][DPL];
     float m[G], l[G];
     float acc[G][DPL];
-    uint32_t lane_off;   // byte offset of this lane's dims inside a row (before swizzle)
 
     __device__ __forceinline__ void load_q(const uint8_t* qbuf, int group, int lane) {
         const uint16_t* q16 = reinterpret_cast<const uint16_t*>(qbuf);
@@ -378,8 +559,7 @@ struct CoreConsumer {
     // Loads this lane's DPL elements of row t of a swizzled tile as fp32.
     __device__ __forceinline__ void load_row(const uint8_t* tile, int t, int lane, float (&x)[DPL]) {
         const int byte = lane * DPL * 2;          // offset inside the unswizzled row
-        const int c16 = byte >> 4;
-        const uint8_t* ptr = tile + swz<C>(t, c16) + (byte & 15);
+        const uint8_t* ptr = tile + swz<C>(t, byte >> 4) + (byte & 15);
         if constexpr (DPL == 4) {
             const uint2 w = *reinterpret_cast<const uint2*>(ptr);
             unpack2<C::kBf16>(w.x, x[0], x[1]);
@@ -391,11 +571,12 @@ struct CoreConsumer {
     }
 
     __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid,
-                                         float scale_log2, int lane, float (*pbuf)[8]) {
+                                         float scale_log2, int lane, float (*pbuf)[BS]) {
+        // 1. logits: chunk tc of 8 tokens leaves token tc*8 + (lane >> 2) in this lane
+        float lg[G][NC8];
+        const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
 #pragma unroll
-        for (int tc = 0; tc < BS / 8; ++tc) {
-            const int nvalid = valid - tc * 8;   // valid tokens in this chunk of 8
-            if (nvalid <= 0) break;
+        for (int tc = 0; tc < NC8; ++tc) {
             float part[G][8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -409,10 +590,7 @@ struct CoreConsumer {
                     part[h][u] = s;
                 }
             }
-            // transposed butterfly: afterwards lane holds the full dot product of token
-            // (lane >> 2) of the chunk, for every head
-            const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
-            float logit[G];
+            // transposed butterfly over the 32 lanes (9 shuffles for 8 tokens)
 #pragma unroll
             for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -435,49 +613,77 @@ struct CoreConsumer {
                 float s = part[h][0];
                 s += __shfl_xor_sync(0xffffffffu, s, 2);
                 s += __shfl_xor_sync(0xffffffffu, s, 1);
-                logit[h] = ((lane >> 2) < nvalid) ? s * scale_log2 : -INFINITY;
+                lg[h][tc] = (tc * 8 + (lane >> 2) < valid) ? s * scale_log2 : -INFINITY;
             }
-            // online softmax update per head
+        }
+        // 2. online softmax update, once per tile
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float mx = logit[h];
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m[h], mx);
-                const float alpha = fast_exp2(m[h] - mn);
-                m[h] = mn;
-                const float e = fast_exp2(logit[h] - mn);
-                l[h] = l[h] * alpha + e;       // per-lane share; summed over tokens at the end
+        for (int h = 0; h < G; ++h) {
+            float mx = lg[h][0];
 #pragma unroll
-                for (int j = 0; j < DPL; ++j) acc[h][j] *= alpha;
-                if ((lane & 3) == 0) pbuf[h][lane >> 2] = e;
+            for (int tc = 1; tc < NC8; ++tc) mx = fmaxf(mx, lg[h][tc]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m[h], mx);
+            const float alpha = fast_exp2(m[h] - mn);
+            m[h] = mn;
+            float ps = 0.f;
+#pragma unroll
+            for (int tc = 0; tc < NC8; ++tc) {
+                const float e = fast_exp2(lg[h][tc] - mn);
+                ps += e;
+                if ((lane & 3) == 0) pbuf[h][tc * 8 + (lane >> 2)] = e;
             }
-            __syncwarp();
-            float pw[G][8];
+            l[h] = l[h] * alpha + ps;        // per-lane share; summed over lanes at the end
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float4 a = *reinterpret_cast<const float4*>(&pbuf[h][0]);
-                const float4 b = *reinterpret_cast<const float4*>(&pbuf[h][4]);
-                pw[h][0] = a.x; pw[h][1] = a.y; pw[h][2] = a.z; pw[h][3] = a.w;
-                pw[h][4] = b.x; pw[h][5] = b.y; pw[h][6] = b.z; pw[h][7] = b.w;
-            }
-            __syncwarp();
+            for (int j = 0; j < DPL; ++j) acc[h][j] *= alpha;
+        }
+        __syncwarp();
+        // 3. P V over the valid rows (rows past the context are never touched)
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (u < nvalid) {   // rows past the context are never touched
-                    float v[DPL];
-                    load_row(vt, tc * 8 + u, lane, v);
+        for (int t = 0; t < BS; ++t) {
+            if (t < valid) {
+                float v[DPL];
+                load_row(vt, t, lane, v);
 #pragma unroll
-                    for (int h = 0; h < G; ++h)
+                for (int h = 0; h < G; ++h) {
+                    const float w = pbuf[h][t];
 #pragma unroll
-                        for (int j = 0; j < DPL; ++j) acc[h][j] = fmaf(pw[h][u], v[j], acc[h][j]);
+                    for (int j = 0; j < DPL; ++j) acc[h][j] = fmaf(w, v[j], acc[h][j]);
                 }
             }
         }
+        __syncwarp();
     }
 
-    __device__ __forceinline__ void finish(float* ostage, const DecodeParams& p, const UnitDesc& u,
+    __device__ __forceinline__ void export_state(float* buf, int lane) const {
+        int k = 0;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            buf[(k++) * 32 + lane] = m[h];
+            buf[(k++) * 32 + lane] = l[h];
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) buf[(k++) * 32 + lane] = acc[h][j];
+        }
+    }
+
+    __device__ __forceinline__ void merge_state(const float* buf, int lane) {
+        int k = 0;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float mo = buf[(k++) * 32 + lane];
+            const float lo = buf[(k++) * 32 + lane];
+            const float M = fmaxf(m[h], mo);
+            const float a = state_weight(m[h], M), b = state_weight(mo, M);
+            m[h] = M;
+            l[h] = a * l[h] + b * lo;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) acc[h][j] = a * acc[h][j] + b * buf[(k++) * 32 + lane];
+        }
+    }
+
+    __device__ __forceinline__ void finish(float*, const DecodeParams& p, const UnitDesc& u,
                                            int lane) {
         const bool final_out = u.pslot < 0;
         const int g = p.group;
@@ -513,7 +719,7 @@ struct CoreConsumer {
                     p.part_ml[(size_t)u.pslot * p.num_q_heads + row] = make_float2(m[h], lt);
             }
         }
-        (void)ostage;
+        if (!final_out) finish_partition<C>(p, u, lane);
     }
 };
 
@@ -539,59 +745,83 @@ __global__ void __launch_bounds__(C::THREADS)
         }
         for (int i = 0; i < C::NQ; ++i) {
             mbar_init(&sm.qfull[i], 1);
-            mbar_init(&sm.qempty[i], 1);
+            mbar_init(&sm.qempty[i], C::NCONS);
             sm.qissued[i] = 0;
             sm.qconsumed[i] = 0;
         }
         sm.abort = 0;
         fence_barrier_init();
+        prefetch_tensor_map(&kmap);
+        prefetch_tensor_map(&vmap);
     }
     __syncthreads();
+    // Launched as a programmatic dependent of the plan (V2) or reshape (V1) kernel: the
+    // set-up above overlaps the predecessor; nothing it writes is read before this.
+    grid_dependency_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tensor_map(&kmap);
-            prefetch_tensor_map(&vmap);
-        }
         const uint64_t policy = l2_evict_first_policy();
         const int32_t total = persistent ? (int32_t)p.hdr->total_units : num_units_v1;
+        // V2: the partition size the plan kernel settled on (fixed or adaptive)
+        const int32_t P = persistent ? (int32_t)p.hdr->partition_size : 0;
         const int32_t Hkv = p.num_kv_heads, g = p.group;
         const uint32_t qbytes = (uint32_t)(g * C::D * 2);
-        uint32_t stage = 0, ephase = 1;
-        bool first = true;
-        for (uint32_t it = 0;; ++it) {
-            int32_t w;
-            if (persistent) {
-                int32_t c = 0;
-                if (lane == 0) c = (int32_t)atomicAdd(&p.hdr->counter, 1u);
-                w = __shfl_sync(0xffffffffu, c, 0);
-            } else {
-                w = first ? (int32_t)blockIdx.x : total;
-            }
-            first = false;
-            const bool done = w >= total || sm.abort;
+        // Unit w as a descriptor: V1 units are (sequence, kv head) from the grid index;
+        // V2 units come from the plan's list entry e (seq, partition, base slot, length).
+        auto describe = [&](int32_t w, int4 e, bool done) {
             UnitDesc u;
             u.seq = -1;
             u.kvh = 0;
             u.tok0 = 0;
             u.tok1 = 0;
             u.pslot = -1;
+            u.pbase = 0;
+            u.nparts = 1;
+            u.pad = 0;
             if (!done) {
                 u.kvh = w % Hkv;
-                if (p.partition_size == 0) {
+                if (!persistent) {
                     u.seq = w / Hkv;
                     u.tok1 = clamped_len(p, u.seq, u.kvh == 0);
                 } else {
-                    const int32_t j = w / Hkv;
-                    const int2 e = p.part_list[j];
                     u.seq = e.x;
-                    const int32_t L = clamped_len(p, u.seq, false);
-                    u.tok0 = e.y * p.partition_size;
-                    u.tok1 = min(u.tok0 + p.partition_size, L);
-                    u.pslot = L > p.partition_size ? j : -1;
+                    u.tok0 = e.y * P;
+                    u.tok1 = min(u.tok0 + P, e.w);
+                    u.nparts = e.w > 0 ? (e.w + P - 1) / P : 1;
+                    u.pbase = e.z;
+                    u.pslot = u.nparts > 1 ? e.z + e.y : -1;
                 }
             }
+            return u;
+        };
+        // Loads (all lanes, one entry each) block-table entries b0 .. b0+31 of a unit,
+        // replacing entries outside the pool by a row past the tensor map (TMA reads zeros).
+        auto load_blocks = [&](const UnitDesc& u, int32_t b0, int32_t n) {
+            int32_t phys = 0;
+            if (lane < n) {
+                phys = p.block_tables[(size_t)u.seq * p.max_blocks_per_seq + b0 + lane];
+                if (phys < 0 || phys >= p.num_blocks) {
+                    if (u.kvh == 0) flag_error(p.status, PA_DEVERR_BAD_BLOCK_);
+                    phys = p.num_blocks;
+                }
+            }
+            return phys;
+        };
+        const int4 kNoEntry = make_int4(0, 0, 0, 0);
+        // The first unit.  Later units are claimed one ahead: the atomic, the list entry
+        // and the first block-table entries of unit k+1 are fetched while unit k's tiles
+        // are issued, so that a new unit does not start with three dependent loads.
+        int32_t claimed = 0;   // lane 0: raw result of the last atomic claim
+        if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+        int32_t w = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : (int32_t)blockIdx.x;
+        int4 e = (persistent && w < total) ? p.part_list[w / Hkv] : kNoEntry;
+        int32_t pre_phys = 0;       // prefetched first block-table chunk of unit w
+        bool have_pre = false;
+        uint32_t stage = 0, ephase = 1;
+        for (uint32_t it = 0;; ++it) {
+            const bool done = w >= total || warp_sees_abort(sm.abort);
+            const UnitDesc u = describe(w, e, done);
             const uint32_t qs = it % C::NQ, qphase = ((it / C::NQ) & 1) ^ 1;
             bool ok = true;
             if (lane == 0) {
@@ -618,18 +848,38 @@ __global__ void __launch_bounds__(C::THREADS)
                 break;
             }
             if (u.seq < 0) break;
+            // The next unit is claimed once at most kClaimLead of this unit's tiles are left
+            // to issue: early enough that its claim, list entry and first block-table
+            // entries arrive before they are needed, late enough that a CTA does not sit on
+            // a claimed unit that an idle CTA could have taken (which hurts the balance when
+            // units are long).  Steps: 0 unclaimed, 1 claimed, 2 entry loaded, 3 blocks loaded.
+            constexpr int32_t kClaimLead = PA_CLAIM_LEAD;
+            int32_t w_next = total;
+            int4 e_next = kNoEntry;
+            int32_t next_phys = 0;
+            int step = 0;
+            auto advance_next = [&]() {
+                if (step == 0) {
+                    if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+                    step = 1;
+                } else if (step == 1) {
+                    w_next = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : total;
+                    e_next = (persistent && w_next < total) ? p.part_list[w_next / Hkv] : kNoEntry;
+                    step = 2;
+                } else if (step == 2) {
+                    if (w_next < total) {
+                        const UnitDesc un = describe(w_next, e_next, false);
+                        const int32_t nb0 = un.tok0 / C::BS, nb1 = (un.tok1 + C::BS - 1) / C::BS;
+                        next_phys = load_blocks(un, nb0, min(32, nb1 - nb0));
+                    }
+                    step = 3;
+                }
+            };
             const int32_t b0 = u.tok0 / C::BS, b1 = (u.tok1 + C::BS - 1) / C::BS;
-            const int32_t* bt_row = p.block_tables + (size_t)u.seq * p.max_blocks_per_seq;
+            if (b1 - b0 <= kClaimLead) advance_next();
             for (int32_t jb = b0; jb < b1 && ok; jb += 32) {
                 const int32_t n = min(32, b1 - jb);
-                int32_t phys = 0;
-                if (lane < n) {
-                    phys = bt_row[jb + lane];
-                    if (phys < 0 || phys >= p.num_blocks) {
-                        if (u.kvh == 0) flag_error(p.status, PA_DEVERR_BAD_BLOCK_);
-                        phys = p.num_blocks;   // past the tensor map's rows: TMA fills zeros
-                    }
-                }
+                const int32_t phys = (jb == b0 && have_pre) ? pre_phys : load_blocks(u, jb, n);
                 for (int32_t i = 0; i < n; ++i) {
                     const int32_t pb = __shfl_sync(0xffffffffu, phys, i);
                     if (lane == 0) {
@@ -653,6 +903,7 @@ __global__ void __launch_bounds__(C::THREADS)
                         stage = 0;
                         ephase ^= 1;
                     }
+                    if (step > 0 || b1 - (jb + i + 1) <= kClaimLead) advance_next();
                 }
             }
             if (!ok) {
@@ -662,61 +913,74 @@ __global__ void __launch_bounds__(C::THREADS)
                 }
                 break;
             }
+            while (step < 3) advance_next();
+            w = w_next;
+            e = e_next;
+            pre_phys = next_phys;
+            have_pre = w < total;
         }
     } else {
-        // ------------------------------------------------------------ consumer
+        // ------------------------------------------------------------ consumers
         using Consumer = typename std::conditional<C::kMma, MmaConsumer<C>, CoreConsumer<C>>::type;
+        const int c = warp - 1;
+        constexpr int kConsThreads = 32 * C::NCONS;
+        // A decision every consumer thread must take the same way (abort or go on).
+        auto all_agree = [&](bool v) {
+            if constexpr (C::NCONS > 1) return consumers_any(v, kConsThreads);
+            else return __any_sync(0xffffffffu, v);
+        };
         Consumer cons;
-        uint32_t stage = 0, fphase = 0;
+        uint32_t gtile = 0;   // tiles of all earlier units, counted over every consumer
         for (uint32_t it = 0;; ++it) {
             const uint32_t qs = it % C::NQ, qphase = (it / C::NQ) & 1;
-            if (!mbar_wait(&sm.qfull[qs], qphase)) {
-                if (lane == 0) {
-                    flag_error(p.status, PA_DEVERR_TIMEOUT_);
-                    sm.abort = 1;
-                }
-                break;
+            const bool ok = mbar_wait_warp(&sm.qfull[qs], qphase);
+            if (!ok && lane == 0) {
+                flag_error(p.status, PA_DEVERR_TIMEOUT_);
+                sm.abort = 1;
             }
+            if (all_agree(!ok || sm.abort != 0)) break;
             const UnitDesc u = sm.unit[qs];
             if (u.seq < 0) break;
             cons.load_q(sm.qbuf[qs], p.group, lane);
             __syncwarp();
             if (lane == 0) {
-                sm.qconsumed[qs] += 1;
+                if (c == 0) sm.qconsumed[qs] += 1;
                 mbar_arrive(&sm.qempty[qs]);
             }
             cons.reset();
             const int32_t b0 = u.tok0 / C::BS, b1 = (u.tok1 + C::BS - 1) / C::BS;
-            bool ok = true;
-            for (int32_t b = b0; b < b1; ++b) {
-                if (!mbar_wait(&sm.full[stage], fphase)) {
-                    ok = false;
+            const int32_t ntiles = b1 - b0;
+            for (int32_t j = c; j < ntiles; j += C::NCONS) {
+                const uint32_t k = gtile + (uint32_t)j;
+                const uint32_t stage = k % C::NSTAGE, fphase = (k / C::NSTAGE) & 1;
+                if (warp_sees_abort(sm.abort)) break;
+                if (!mbar_wait_warp(&sm.full[stage], fphase)) {
+                    if (lane == 0) {
+                        flag_error(p.status, PA_DEVERR_TIMEOUT_);
+                        sm.abort = 1;
+                    }
                     break;
                 }
-                const int valid = min(C::BS, u.tok1 - b * C::BS);
-                if constexpr (C::kMma) {
-                    cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, p.scale_log2, lane);
-                } else {
-                    cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, p.scale_log2, lane, sm.pbuf);
-                }
+                const int valid = min(C::BS, u.tok1 - (b0 + j) * C::BS);
+                cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, p.scale_log2, lane, sm.pbuf[c]);
                 __syncwarp();
                 if (lane == 0) {
                     sm.consumed[stage] += 1;
                     mbar_arrive(&sm.empty[stage]);
                 }
-                if (++stage == C::NSTAGE) {
-                    stage = 0;
-                    fphase ^= 1;
+            }
+            gtile += (uint32_t)ntiles;
+            if constexpr (C::NCONS > 1) {
+                if (c > 0) cons.export_state(sm.xbuf[c - 1], lane);
+                (void)consumers_any(false, kConsThreads);   // states are in shared memory
+                if (c == 0) {
+#pragma unroll
+                    for (int o = 1; o < C::NCONS; ++o) cons.merge_state(sm.xbuf[o - 1], lane);
                 }
             }
-            if (!ok) {
-                if (lane == 0) {
-                    flag_error(p.status, PA_DEVERR_TIMEOUT_);
-                    sm.abort = 1;
-                }
-                break;
-            }
-            cons.finish(sm.ostage, p, u, lane);
+            if (c == 0 && !warp_sees_abort(sm.abort)) cons.finish(sm.ostage, p, u, lane);
+            // also frees xbuf for the next unit
+            if (all_agree(sm.abort != 0)) break;
         }
     }
 

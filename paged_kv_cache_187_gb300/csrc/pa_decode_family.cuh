@@ -6,21 +6,38 @@
 
 #include "pa_decode.cuh"
 
+#ifndef PA_MMA_CONSUMERS
+#define PA_MMA_CONSUMERS 1
+#endif
+#ifndef PA_CORE_CONSUMERS
+#define PA_CORE_CONSUMERS 2
+#endif
+
 namespace pa {
 
-// Ring depth: about 48 KB of K+V stages per CTA, 2..8 stages.
-template <int D, int BS>
+// Ring depth: about 48 KB of K+V stages per CTA, 2..8 stages, rounded up to a multiple
+// of the consumer warps (see DecodeCfg).
+template <int D, int BS, int NCONS>
 constexpr int stages_for() {
     constexpr int per = 2 * D * BS * 2;
-    constexpr int n = 49152 / per;
-    return n < 2 ? 2 : (n > 8 ? 8 : n);
+    constexpr int n0 = 49152 / per;
+    constexpr int n = n0 < 2 ? 2 : (n0 > 8 ? 8 : n0);
+    return ((n + NCONS - 1) / NCONS) * NCONS;
+}
+
+// Consumer warps per CTA: the CUDA-core path needs more warps to keep up with HBM than
+// the tensor-core path does.
+template <bool MMA>
+constexpr int consumers_for() {
+    return MMA ? PA_MMA_CONSUMERS : PA_CORE_CONSUMERS;
 }
 
 template <int D, int BS, bool BF16, bool MMA, int HCAP>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
-    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D, BS>(), 2>;
+    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D, BS, consumers_for<MMA>()>(), 2,
+                        consumers_for<MMA>()>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
     static bool configured = false;   // per instantiation; attribute setting is idempotent
@@ -37,8 +54,19 @@ cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
         return e;
     }
     if (num_units <= 0) return cudaSuccess;
-    kern<<<num_units, C::THREADS, smem, stream>>>(kmap, vmap, p, persistent ? 1 : 0, num_units);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the CTAs may become resident and initialise while the
+    // preceding plan / reshape kernel still runs; the kernel waits for it before reading.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_units);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p, (int32_t)(persistent ? 1 : 0), num_units);
 }
 
 template <int D, bool BF16>

@@ -252,7 +252,8 @@ pa_status run_v1(const DecodeArgs& a) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t ws_bytes) {
+pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t ws_bytes,
+                 bool adaptive = false) {
     pa_status st = check_decode(a);
     if (st != PA_OK) return st;
     if (partition_size <= 0 || partition_size % a.block_size)
@@ -272,10 +273,11 @@ pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t w
     if ((st = make_maps(a, &km, &vm)) != PA_OK) return st;
     pa::DecodeParams p = base_params(a);
     p.partition_size = partition_size;
+    p.adaptive = adaptive ? 1 : 0;
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.hdr = reinterpret_cast<pa::WsHeader*>(w + L.hdr);
-    p.part_offset = reinterpret_cast<int32_t*>(w + L.part_offset);
-    p.part_list = reinterpret_cast<int2*>(w + L.part_list);
+    p.part_list = reinterpret_cast<int4*>(w + L.part_list);
+    p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
     p.part_ml = reinterpret_cast<float2*>(w + L.part_ml);
     p.part_acc = reinterpret_cast<float*>(w + L.part_acc);
     const pa::KernelKey k = kernel_key(a);
@@ -285,14 +287,11 @@ pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t w
         std::max<int64_t>(1, ((int64_t)a.max_context_len + partition_size - 1) / partition_size);
     const int64_t max_units = (int64_t)a.num_seqs * max_parts_per_seq * a.num_kv_heads;
     const int32_t grid = (int32_t)std::min<int64_t>((int64_t)per_sm * di.sms, max_units);
+    p.grid_ctas = grid;
     cudaError_t e = pa::launch_plan(p, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_v2 plan launch");
     e = timed_decode(k, km, vm, p, true, grid, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_v2 launch");
-    if (a.max_context_len > partition_size) {   // some sequence may span several partitions
-        e = pa::launch_reduce(p, a.head_size, k.bf16, a.stream);
-        if (e != cudaSuccess) return cuda_fail(e, "decode_v2 reduce launch");
-    }
     return ok();
 }
 
@@ -310,14 +309,11 @@ void auto_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t block_size,
         *psize = 0;
         return;
     }
-    int32_t P = 512;
-    // Keep at least ~8 units per SM so the last wave is short.
-    while (P > 2 * block_size && P > 64 &&
-           units * std::max<int64_t>(1, (max_context_len + P - 1) / P) < 8LL * di.sms)
-        P /= 2;
-    P = std::max(block_size, (P / block_size) * block_size);
+    // V2 with adaptive partitions: the plan kernel picks the partition size on the
+    // device from the real lengths; 256 tokens is the smallest it may choose, which
+    // bounds the workspace.
     *variant = 2;
-    *psize = P;
+    *psize = std::max(block_size, (256 / block_size) * block_size);
 }
 
 }  // namespace
@@ -338,10 +334,10 @@ WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32
     size_t off = 0;
     L.hdr = off;
     off = align256(off + sizeof(WsHeader));
-    L.part_offset = off;
-    off = align256(off + sizeof(int32_t) * (size_t)(num_seqs + 1));
     L.part_list = off;
-    off = align256(off + sizeof(int2) * (size_t)parts);
+    off = align256(off + sizeof(int4) * (size_t)parts);
+    L.arrive = off;   // [num_seqs][num_kv_heads] used; sized by num_q_heads >= num_kv_heads
+    off = align256(off + sizeof(int32_t) * (size_t)num_seqs * (size_t)num_q_heads);
     L.part_ml = off;
     off = align256(off + sizeof(float2) * (size_t)parts * (size_t)num_q_heads);
     L.part_acc = off;
@@ -466,7 +462,7 @@ pa_status pa_decode_auto(void* out, const void* query, const void* key_cache,
                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                  num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
     if (v == 1) return run_v1(a);
-    return run_v2(a, P, workspace, workspace_bytes);
+    return run_v2(a, P, workspace, workspace_bytes, /*adaptive=*/true);
 }
 
 pa_status pa_decode_step(void* out, const void* query, const void* key, const void* value,

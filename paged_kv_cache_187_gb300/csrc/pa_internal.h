@@ -12,10 +12,11 @@ namespace pa {
 // Head of the V2 workspace.  The plan kernel writes it; the decode kernel's persistent
 // CTAs claim work units from `counter`.
 struct WsHeader {
-    uint32_t counter;      // next unclaimed work unit
-    uint32_t total_units;  // partitions * num_kv_heads
-    uint32_t total_parts;  // partitions over all sequences
-    uint32_t pad[61];
+    uint32_t counter;         // next unclaimed work unit
+    uint32_t total_units;     // partitions * num_kv_heads
+    uint32_t total_parts;     // partitions over all sequences
+    uint32_t partition_size;  // tokens per partition used by this call
+    uint32_t pad[60];
 };
 
 struct DecodeParams {
@@ -29,18 +30,22 @@ struct DecodeParams {
     int32_t block_size;
     int32_t max_context_len;
     float scale_log2;             // softmax scale * log2(e): logits live in base-2 units
-    int32_t partition_size;       // tokens per work unit; 0 = the whole context (V1)
+    int32_t partition_size;       // V2: tokens per partition (the smallest allowed when
+                                  // adaptive); 0 = the whole context per unit (V1)
+    int32_t adaptive;             // V2: 1 = the plan kernel sizes partitions from the lengths
+    int32_t grid_ctas;            // V2: persistent CTAs of the decode launch
     // V2 workspace pieces (null for V1)
     WsHeader* hdr;
-    int32_t* part_offset;         // [S + 1] first partition index of each sequence
-    int2* part_list;              // [parts] (sequence, partition) of each partition
+    int4* part_list;              // [parts] work order: (sequence, partition, first partition
+                                  // slot of the sequence, clamped context length)
+    int32_t* arrive;              // [S][Hkv] partitions of (sequence, kv head) finished so far
     float* part_acc;              // [parts][Hq][D] unnormalised partial outputs
     float2* part_ml;              // [parts][Hq] (running max in base-2 units, exp-sum)
     int32_t* status;              // optional device error word
 };
 
 struct WorkspaceLayout {
-    size_t hdr, part_offset, part_list, part_ml, part_acc, total;
+    size_t hdr, part_list, arrive, part_ml, part_acc, total;
 };
 
 WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
@@ -61,8 +66,6 @@ cudaError_t launch_decode(const KernelKey& key, const CUtensorMap& kmap, const C
                           const DecodeParams& p, bool persistent, int32_t num_units,
                           cudaStream_t stream);
 cudaError_t launch_plan(const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_reduce(const DecodeParams& p, int32_t head_size, bool bf16,
-                          cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int32_t* slot_mapping,
                                      int32_t num_tokens, int32_t num_kv_heads,
