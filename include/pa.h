@@ -175,6 +175,28 @@ pa_status pa_decode_step(void* out, const void* query, const void* key, const vo
                          pa_dtype dtype, void* workspace, size_t workspace_bytes,
                          int32_t* status_dev, pa_stream stream);
 
+/* The same step from HOST buffers, for callers whose step inputs live in host memory:
+ * copies query [S][Hq][D], key / value [S][Hkv][D], slot_mapping [S], block_tables
+ * [S][max_blocks_per_seq] and context_lens [S] from host memory into `staging` (device,
+ * 256-byte aligned, >= pa_decode_step_host_staging_size bytes) with one cudaMemcpyAsync
+ * each, runs pa_decode_step on the staged copies, and copies out [S][Hq][D] back into
+ * out_host.  Everything is enqueued on `stream`; the call does not wait: out_host is valid
+ * once the stream has been synchronised.  Host buffers should be page-locked (pinned) for
+ * the copies to be asynchronous; pageable buffers work but make the copies synchronous.
+ * The pools stay on the device (they are the cache). */
+size_t pa_decode_step_host_staging_size(int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t num_kv_heads, int32_t head_size,
+                                        int32_t max_blocks_per_seq);
+pa_status pa_decode_step_host(void* out_host, const void* query_host, const void* key_host,
+                              const void* value_host, const int32_t* slot_mapping_host,
+                              const int32_t* block_tables_host, const int32_t* context_lens_host,
+                              void* key_cache, void* value_cache, int32_t max_blocks_per_seq,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, int32_t block_size, int32_t num_blocks,
+                              int32_t max_context_len, float scale, pa_dtype dtype,
+                              void* staging, size_t staging_bytes, void* workspace,
+                              size_t workspace_bytes, int32_t* status_dev, pa_stream stream);
+
 /* Compute path for grouped-query attention (group >= 2): 1 (default) contracts the
  * group's query heads with each K/V tile on the tensor cores (mma.sync m16n8k16, fp32
  * accumulate); 0 uses the CUDA-core path that multi-head attention always takes.
@@ -212,6 +234,28 @@ pa_status pa_decode_v2_noalloc(void* out, const void* query, const void* key_cac
                                int32_t max_context_len, float scale, pa_dtype dtype,
                                int32_t partition_size, int32_t* status_dev, pa_stream stream);
 
+/* advance_step [PR]: moves every sequence of a multi-step decode loop to its next token
+ * on the device, with no host round trip between the steps:
+ *   pos = context_lens[s];  context_lens[s] = pos + 1;
+ *   slot_mapping[s] = block_tables[s][pos / block_size] * block_size + pos % block_size;
+ *   input_positions[s] = pos            (if input_positions is not NULL);
+ *   input_tokens[s] = sampled_token_ids[s]  (if both are not NULL).
+ * context_lens enters as the lengths BEFORE the step's token and leaves counting it, the
+ * convention pa_decode_* expects.  The block holding pos must already be in the table:
+ * reserve the loop's blocks with pa_alloc_reserve_batch first.  A missing block gives
+ * slot -1 (reshape_and_cache skips it) and sets PA_DEVERR_BAD_BLOCK.  A single small
+ * kernel; safe to capture in a CUDA graph with the rest of the loop. */
+pa_status pa_advance_step(int32_t* context_lens, int32_t* slot_mapping, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, int32_t num_seqs, int32_t block_size,
+                          int32_t num_blocks, int64_t* input_positions, int64_t* input_tokens,
+                          const int64_t* sampled_token_ids, int32_t* status_dev, pa_stream stream);
+
+/* Self-test of the failure path: launches a one-warp kernel that waits on a pipeline
+ * barrier nobody arrives on, gives up after limit_us (1 .. 2,000,000) microseconds and
+ * ORs PA_DEVERR_TIMEOUT into *status_dev, exactly as the decode kernel does when a copy
+ * never completes.  The kernel returns normally; the context stays usable. */
+pa_status pa_selftest_wait_timeout(int32_t* status_dev, uint32_t limit_us, pa_stream stream);
+
 /* Profiling hook: when both are non-NULL (cudaEvent_t handles), every later decode
  * call records `start_event` on its stream right before it launches the paged decode
  * kernel and `stop_event` right after, so that the kernel alone can be timed with
@@ -226,8 +270,8 @@ pa_status pa_set_kernel_events(void* start_event, void* stop_event);
  * num_blocks-1 down to 1, j = r % (i+1), r the next splitmix64 output seeded with
  * `seed`); the result is the free list, popped from its end.  add_seq pops
  * ceil(num_tokens / block_size) blocks in logical order; append pops one block when
- * the length is a multiple of block_size, then returns the slot of the new last
- * position; free_seq pushes the blocks back in logical order.  A request that needs
+ * the new position has no block yet (none reserved ahead), then returns the slot of the
+ * new last position; free_seq pushes the blocks back in logical order.  A request that needs
  * more blocks than are free returns PA_ERR_NO_BLOCKS and changes nothing. */
 typedef struct pa_alloc pa_alloc;
 
@@ -242,6 +286,11 @@ pa_status pa_alloc_append(pa_alloc* alloc, int32_t seq_id, int32_t* slot_out);
 /* Appends one token to each of n sequences (all or nothing); slots_out[i] = slot. */
 pa_status pa_alloc_append_batch(pa_alloc* alloc, const int32_t* seq_ids, int32_t n,
                                 int32_t* slots_out);
+/* Reserves blocks ahead for a multi-step loop: each listed sequence gets blocks until it
+ * owns ceil((len + extra_tokens) / block_size) of them, popped in list order; lengths do
+ * not change, and later appends use the reserved blocks first.  All or nothing. */
+pa_status pa_alloc_reserve_batch(pa_alloc* alloc, const int32_t* seq_ids, int32_t n,
+                                 int32_t extra_tokens);
 /* Returns seq_id's blocks to the free list and forgets the sequence. */
 pa_status pa_alloc_free_seq(pa_alloc* alloc, int32_t seq_id);
 /* Slots of positions [start, start + n) of seq_id. */

@@ -97,6 +97,8 @@ def _load():
         lib.or_alloc_add_seq.restype = i32
         lib.or_alloc_append.argtypes = [P, i32, ctypes.POINTER(i32)]
         lib.or_alloc_append.restype = i32
+        lib.or_alloc_reserve.argtypes = [P, i32, i32]
+        lib.or_alloc_reserve.restype = i32
         lib.or_alloc_free_seq.argtypes = [P, i32]
         lib.or_alloc_free_seq.restype = i32
         lib.or_alloc_slots.argtypes = [P, i32, i32, i32, P]
@@ -246,6 +248,9 @@ class Alloc:
         slot = ctypes.c_int32(0)
         self._chk(self._lib.or_alloc_append(self._h, seq_id, ctypes.byref(slot)))
         return int(slot.value)
+
+    def reserve(self, seq_id: int, extra_tokens: int):
+        self._chk(self._lib.or_alloc_reserve(self._h, seq_id, extra_tokens))
 
     def free_seq(self, seq_id: int):
         self._chk(self._lib.or_alloc_free_seq(self._h, seq_id))

@@ -329,8 +329,9 @@ int32_t or_paged_decode_v2(double* out, const uint16_t* q, const uint16_t* k_cac
 /*     r the next splitmix64 output of a generator seeded with `seed`.          */
 /*  2. The shuffled array is the free list; blocks are popped from its end.     */
 /*  3. add_seq(id, n) pops ceil(n / block_size) blocks, in logical order.       */
-/*  4. append(id) pops one block first when the length is a multiple of         */
-/*     block_size, then returns the slot of position len and increments len.   */
+/*  4. append(id) pops one block first when position len has no block yet      */
+/*     (len a multiple of block_size, nothing reserved ahead), then returns the */
+/*     slot of position len and increments len.                                 */
 /*  5. free_seq(id) pushes the sequence's blocks back in logical order.         */
 /*  6. A request that needs more blocks than are free fails and changes         */
 /*     nothing.                                                                */
@@ -416,12 +417,27 @@ int32_t or_alloc_add_seq(or_alloc* a, int32_t id, int32_t num_tokens) {
 int32_t or_alloc_append(or_alloc* a, int32_t id, int32_t* slot) {
     if (id < 0 || id >= a->max_seqs || !a->live[id]) return -1;
     int32_t L = a->len[id];
-    if (L % a->block_size == 0) {
+    if (L / a->block_size >= a->nblocks[id]) {   /* position L needs a block not yet owned */
         if (a->num_free == 0) return -3;
         push_block(a, id, a->free_list[--a->num_free]);
     }
     *slot = a->blocks[id][L / a->block_size] * a->block_size + L % a->block_size;
     a->len[id] = L + 1;
+    return 0;
+}
+
+/* Lookahead reservation for a multi-step loop ([PR]: several decode steps run before the
+ * scheduler sees the batch again, so their blocks must exist up front).  Spec, same on
+ * both sides: reserve(id, extra) pops blocks, in logical order, until the sequence owns
+ * ceil((len + extra) / block_size) blocks; len is unchanged.  Returns 0, -1, -3 (not
+ * enough free blocks; nothing changed). */
+int32_t or_alloc_reserve(or_alloc* a, int32_t id, int32_t extra) {
+    if (id < 0 || id >= a->max_seqs || !a->live[id] || extra < 0) return -1;
+    int32_t want = (a->len[id] + extra + a->block_size - 1) / a->block_size;
+    int32_t need = want - a->nblocks[id];
+    if (need <= 0) return 0;
+    if (need > a->num_free) return -3;
+    for (int32_t i = 0; i < need; ++i) push_block(a, id, a->free_list[--a->num_free]);
     return 0;
 }
 

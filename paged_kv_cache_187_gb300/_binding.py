@@ -57,6 +57,7 @@ def _load():
         "pa_version": ([], i32),
         "pa_set_gqa_tensor_cores": ([i32], i32),
         "pa_set_kernel_events": ([P, P], i32),
+        "pa_selftest_wait_timeout": ([P, ctypes.c_uint32, P], i32),
         "pa_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
         "pa_decode_v1": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P],
                          i32),
@@ -72,6 +73,9 @@ def _load():
                             sz, P, P], i32),
         "pa_decode_step": ([P, P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
                             i32, P, sz, P, P], i32),
+        "pa_decode_step_host_staging_size": ([i32, i32, i32, i32, i32], sz),
+        "pa_decode_step_host": ([P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                 f32, i32, P, sz, P, sz, P, P], i32),
         "pa_alloc_create": ([i32, i32, u64, ctypes.POINTER(P)], i32),
         "pa_alloc_destroy": ([P], None),
         "pa_alloc_num_free": ([P], i32),
@@ -79,6 +83,8 @@ def _load():
         "pa_alloc_append": ([P, i32, ctypes.POINTER(i32)], i32),
         "pa_alloc_append_batch": ([P, P, i32, P], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
+        "pa_alloc_reserve_batch": ([P, P, i32, i32], i32),
+        "pa_advance_step": ([P, P, P, i32, i32, i32, i32, P, P, P, P, P], i32),
         "pa_alloc_slots": ([P, i32, i32, i32, P], i32),
         "pa_alloc_block_tables": ([P, P, i32, i32, P], i32),
         "pa_alloc_context_lens": ([P, P, i32, P], i32),
@@ -275,6 +281,52 @@ def pa_decode_step(out, query, key, value, key_cache, value_cache, slot_mapping,
         _stream(stream)))
 
 
+def pa_decode_step_host_staging_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                     max_blocks_per_seq) -> int:
+    return int(_lib.pa_decode_step_host_staging_size(num_seqs, num_q_heads, num_kv_heads,
+                                                     head_size, max_blocks_per_seq))
+
+
+def _host(a, name, dtype=None):
+    """Host buffer pointer: a CPU torch tensor or a numpy array, contiguous."""
+    if hasattr(a, "is_cuda"):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+        if dtype is not None and a.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}")
+        return ctypes.c_void_p(a.data_ptr())
+    arr = a
+    if not arr.flags.c_contiguous:
+        raise ValueError(f"{name} must be contiguous")
+    return arr.ctypes.data_as(ctypes.c_void_p)
+
+
+def pa_decode_step_host(out_host, query_host, key_host, value_host, slot_mapping_host,
+                        block_tables_host, context_lens_host, key_cache, value_cache,
+                        max_context_len: int, scale: float, staging, workspace=None,
+                        status=None, stream=None):
+    """One decode step from host buffers (pinned CPU tensors): H2D of the inputs,
+    reshape_and_cache + decode, D2H of out, all enqueued on the stream (no wait)."""
+    import torch
+    S, Hq, D = query_host.shape
+    NB, Hkv, bs, D2 = key_cache.shape
+    if key_host.shape != (S, Hkv, D) or value_host.shape != key_host.shape or D2 != D:
+        raise ValueError("decode_step_host: key/value [S, Hkv, D] expected")
+    if out_host.shape != query_host.shape or tuple(slot_mapping_host.shape) != (S,):
+        raise ValueError("decode_step_host: out [S, Hq, D] and slot_mapping [S] expected")
+    maxb = int(block_tables_host.shape[1])
+    dt = _dt(key_cache)
+    wp, wb = _ws(workspace)
+    sp, sb = _ws(staging)
+    _check(_lib.pa_decode_step_host(
+        _host(out_host, "out_host"), _host(query_host, "query_host"), _host(key_host, "key_host"),
+        _host(value_host, "value_host"), _host(slot_mapping_host, "slot_mapping_host"),
+        _host(block_tables_host, "block_tables_host"), _host(context_lens_host, "context_lens_host"),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), maxb, S, Hq, Hkv, D, bs, NB,
+        int(max_context_len), float(scale), dt, sp, sb, wp, wb, _opt_dev(status, "status"),
+        _stream(stream)))
+
+
 def pa_set_kernel_events(start_event, stop_event):
     """torch.cuda.Event pair (already recorded once, so that the CUDA event exists) or
     (None, None) to switch the hook off."""
@@ -283,6 +335,31 @@ def pa_set_kernel_events(start_event, stop_event):
         return
     _check(_lib.pa_set_kernel_events(ctypes.c_void_p(start_event.cuda_event),
                                      ctypes.c_void_p(stop_event.cuda_event)))
+
+
+def pa_advance_step(context_lens, slot_mapping, block_tables, block_size: int, num_blocks: int,
+                    input_positions=None, input_tokens=None, sampled_token_ids=None,
+                    status=None, stream=None):
+    """Device-side move of every sequence to its next token (multi-step decode loop)."""
+    import torch
+    S = int(context_lens.shape[0])
+    if slot_mapping.shape != (S,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("advance_step: context_lens / slot_mapping [S], block_tables [S, max]")
+    def opt64(t, name):
+        return None if t is None else _dev(t, name, torch.int64)
+    _check(_lib.pa_advance_step(
+        _dev(context_lens, "context_lens", torch.int32), _dev(slot_mapping, "slot_mapping", torch.int32),
+        _dev(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]), S,
+        int(block_size), int(num_blocks), opt64(input_positions, "input_positions"),
+        opt64(input_tokens, "input_tokens"), opt64(sampled_token_ids, "sampled_token_ids"),
+        _opt_dev(status, "status"), _stream(stream)))
+
+
+def pa_selftest_wait_timeout(status, limit_us: int, stream=None):
+    """Runs the bounded-wait self-test kernel; sets PA_DEVERR_TIMEOUT in `status`."""
+    import torch
+    _check(_lib.pa_selftest_wait_timeout(_dev(status, "status", torch.int32), int(limit_us),
+                                         _stream(stream)))
 
 
 def pa_set_gqa_tensor_cores(enable: bool):
@@ -332,11 +409,23 @@ class PagedAllocator:
         _check(_lib.pa_alloc_append(self._h, int(seq_id), ctypes.byref(s)))
         return int(s.value)
 
-    def pa_alloc_append_batch(self, seq_ids) -> np.ndarray:
+    @staticmethod
+    def _out(out, shape):
+        if out is None:
+            return np.empty(shape, dtype=np.int32)
+        if out.dtype != np.int32 or out.shape != tuple(shape) or not out.flags.c_contiguous:
+            raise ValueError(f"out must be a contiguous int32 array of shape {tuple(shape)}")
+        return out
+
+    def pa_alloc_append_batch(self, seq_ids, out=None) -> np.ndarray:
         ids = _np_i32(seq_ids)
-        out = np.empty(ids.size, dtype=np.int32)
+        out = self._out(out, (ids.size,))
         _check(_lib.pa_alloc_append_batch(self._h, _nptr(ids), ids.size, _nptr(out)))
         return out
+
+    def pa_alloc_reserve_batch(self, seq_ids, extra_tokens: int):
+        ids = _np_i32(seq_ids)
+        _check(_lib.pa_alloc_reserve_batch(self._h, _nptr(ids), ids.size, int(extra_tokens)))
 
     def pa_alloc_free_seq(self, seq_id: int):
         _check(_lib.pa_alloc_free_seq(self._h, int(seq_id)))
@@ -346,15 +435,15 @@ class PagedAllocator:
         _check(_lib.pa_alloc_slots(self._h, int(seq_id), int(start), int(n), _nptr(out)))
         return out
 
-    def pa_alloc_block_tables(self, seq_ids, max_blocks_per_seq: int) -> np.ndarray:
+    def pa_alloc_block_tables(self, seq_ids, max_blocks_per_seq: int, out=None) -> np.ndarray:
         ids = _np_i32(seq_ids)
-        out = np.empty((ids.size, int(max_blocks_per_seq)), dtype=np.int32)
+        out = self._out(out, (ids.size, int(max_blocks_per_seq)))
         _check(_lib.pa_alloc_block_tables(self._h, _nptr(ids), ids.size, int(max_blocks_per_seq),
                                           _nptr(out)))
         return out
 
-    def pa_alloc_context_lens(self, seq_ids) -> np.ndarray:
+    def pa_alloc_context_lens(self, seq_ids, out=None) -> np.ndarray:
         ids = _np_i32(seq_ids)
-        out = np.empty(ids.size, dtype=np.int32)
+        out = self._out(out, (ids.size,))
         _check(_lib.pa_alloc_context_lens(self._h, _nptr(ids), ids.size, _nptr(out)))
         return out

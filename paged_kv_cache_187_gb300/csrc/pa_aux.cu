@@ -206,7 +206,67 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     grid_dependency_wait();
 }
 
+// Moves every sequence to its next token on the device, between the steps of a
+// multi-step decode loop ("[core] Multi Step Scheduling #7000": the advance_step op that
+// updates seq_lens, slot_mapping and block_tables in place, with input tokens and
+// positions).  The new token's block must already be in the table: the host reserves
+// the loop's blocks up front.  A missing block leaves the slot at -1 (a padding token:
+// reshape_and_cache then skips it) and flags PA_DEVERR_BAD_BLOCK.
+__global__ void __launch_bounds__(256)
+    advance_step_kernel(int32_t* __restrict__ context_lens, int32_t* __restrict__ slot_mapping,
+                        const int32_t* __restrict__ block_tables, int32_t max_blocks_per_seq,
+                        int32_t num_seqs, int32_t block_size, int32_t num_blocks,
+                        int64_t* __restrict__ input_positions, int64_t* __restrict__ input_tokens,
+                        const int64_t* __restrict__ sampled_token_ids, int32_t* status) {
+    const int32_t s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= num_seqs) return;
+    const int32_t pos = context_lens[s];          // position of the sequence's next token
+    context_lens[s] = pos + 1;
+    if (input_positions) input_positions[s] = pos;
+    if (input_tokens) input_tokens[s] = sampled_token_ids[s];
+    const int32_t logical = pos / block_size;
+    int32_t slot = -1;
+    if (pos >= 0 && logical < max_blocks_per_seq) {
+        const int32_t phys = block_tables[(size_t)s * max_blocks_per_seq + logical];
+        if (phys >= 0 && phys < num_blocks) slot = phys * block_size + pos % block_size;
+    }
+    if (slot < 0 && status) atomicOr(status, 2 /* PA_DEVERR_BAD_BLOCK */);
+    slot_mapping[s] = slot;
+}
+
+// Exercises the bounded pipeline wait: waits on a shared-memory barrier that nothing
+// will ever arrive on, gives up after limit_ns, and reports PA_DEVERR_TIMEOUT exactly as
+// the decode kernel does when a TMA completion never comes.
+__global__ void __launch_bounds__(32) wait_timeout_probe_kernel(int32_t* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_for(&bar, 0, limit_ns);   // phase 0 never completes
+    if (threadIdx.x == 0 && !ok && status) atomicOr(status, 8 /* PA_DEVERR_TIMEOUT */);
+}
+
 }  // namespace
+
+cudaError_t launch_advance_step(int32_t* context_lens, int32_t* slot_mapping,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                int32_t num_seqs, int32_t block_size, int32_t num_blocks,
+                                int64_t* input_positions, int64_t* input_tokens,
+                                const int64_t* sampled_token_ids, int32_t* status,
+                                cudaStream_t stream) {
+    const int32_t threads = 256;
+    advance_step_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
+        context_lens, slot_mapping, block_tables, max_blocks_per_seq, num_seqs, block_size,
+        num_blocks, input_positions, input_tokens, sampled_token_ids, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int32_t* slot_mapping,

@@ -357,6 +357,128 @@ const char* pa_last_error(void) { return g_last_error.c_str(); }
 
 int32_t pa_version(void) { return 100; }
 
+namespace {
+
+// Device staging of pa_decode_step_host: the step's inputs and its output rows.
+struct StagingLayout {
+    size_t out, q, k, v, slots, tables, lens, total;
+};
+
+StagingLayout staging_layout(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t maxb) {
+    StagingLayout L;
+    size_t off = 0;
+    L.out = off;
+    off = align256(off + (size_t)S * Hq * D * 2);
+    L.q = off;
+    off = align256(off + (size_t)S * Hq * D * 2);
+    L.k = off;
+    off = align256(off + (size_t)S * Hkv * D * 2);
+    L.v = off;
+    off = align256(off + (size_t)S * Hkv * D * 2);
+    L.slots = off;
+    off = align256(off + (size_t)S * 4);
+    L.tables = off;
+    off = align256(off + (size_t)S * maxb * 4);
+    L.lens = off;
+    off = align256(off + (size_t)S * 4);
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+size_t pa_decode_step_host_staging_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_size, int32_t max_blocks_per_seq) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+        max_blocks_per_seq <= 0)
+        return 0;
+    return staging_layout(num_seqs, num_q_heads, num_kv_heads, head_size, max_blocks_per_seq).total;
+}
+
+pa_status pa_decode_step_host(void* out_host, const void* query_host, const void* key_host,
+                              const void* value_host, const int32_t* slot_mapping_host,
+                              const int32_t* block_tables_host, const int32_t* context_lens_host,
+                              void* key_cache, void* value_cache, int32_t max_blocks_per_seq,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, int32_t block_size, int32_t num_blocks,
+                              int32_t max_context_len, float scale, pa_dtype dtype, void* staging,
+                              size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                              int32_t* status_dev, pa_stream stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+        max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "decode_step_host: sizes must be positive");
+    if (num_seqs == 0) return ok();
+    if (!out_host || !query_host || !key_host || !value_host || !slot_mapping_host ||
+        !block_tables_host || !context_lens_host)
+        return fail(PA_ERR_INVALID_ARG, "decode_step_host: null host pointer");
+    const StagingLayout L =
+        staging_layout(num_seqs, num_q_heads, num_kv_heads, head_size, max_blocks_per_seq);
+    if (!staging || staging_bytes < L.total)
+        return fail(PA_ERR_WORKSPACE, "decode_step_host: staging of %zu bytes, need %zu",
+                    staging_bytes, L.total);
+    if (reinterpret_cast<uintptr_t>(staging) & 255u)
+        return fail(PA_ERR_INVALID_ARG, "decode_step_host: staging must be 256-byte aligned");
+    uint8_t* st = static_cast<uint8_t*>(staging);
+    cudaStream_t cs = (cudaStream_t)stream;
+    const size_t S = (size_t)num_seqs;
+    struct Copy {
+        void* dst;
+        const void* src;
+        size_t bytes;
+    } copies[] = {
+        {st + L.q, query_host, S * num_q_heads * head_size * 2},
+        {st + L.k, key_host, S * num_kv_heads * head_size * 2},
+        {st + L.v, value_host, S * num_kv_heads * head_size * 2},
+        {st + L.slots, slot_mapping_host, S * 4},
+        {st + L.tables, block_tables_host, S * max_blocks_per_seq * 4},
+        {st + L.lens, context_lens_host, S * 4},
+    };
+    for (const Copy& c : copies) {
+        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: H2D copy");
+    }
+    pa_status ps = pa_decode_step(
+        st + L.out, st + L.q, st + L.k, st + L.v, key_cache, value_cache,
+        reinterpret_cast<const int32_t*>(st + L.slots), reinterpret_cast<const int32_t*>(st + L.tables),
+        max_blocks_per_seq, reinterpret_cast<const int32_t*>(st + L.lens), num_seqs, num_q_heads,
+        num_kv_heads, head_size, block_size, num_blocks, max_context_len, scale, dtype, workspace,
+        workspace_bytes, status_dev, stream);
+    if (ps != PA_OK) return ps;
+    cudaError_t e = cudaMemcpyAsync(out_host, st + L.out, S * num_q_heads * head_size * 2,
+                                    cudaMemcpyDeviceToHost, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: D2H copy");
+    return ok();
+}
+
+pa_status pa_advance_step(int32_t* context_lens, int32_t* slot_mapping, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, int32_t num_seqs, int32_t block_size,
+                          int32_t num_blocks, int64_t* input_positions, int64_t* input_tokens,
+                          const int64_t* sampled_token_ids, int32_t* status_dev, pa_stream stream) {
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "advance_step: sizes must be positive");
+    if (num_seqs == 0) return ok();
+    if (!context_lens || !slot_mapping || !block_tables)
+        return fail(PA_ERR_INVALID_ARG, "advance_step: null pointer");
+    if ((input_tokens == nullptr) != (sampled_token_ids == nullptr))
+        return fail(PA_ERR_INVALID_ARG, "advance_step: input_tokens and sampled_token_ids go together");
+    cudaError_t e = pa::launch_advance_step(context_lens, slot_mapping, block_tables,
+                                            max_blocks_per_seq, num_seqs, block_size, num_blocks,
+                                            input_positions, input_tokens, sampled_token_ids,
+                                            status_dev, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "advance_step launch");
+    return ok();
+}
+
+pa_status pa_selftest_wait_timeout(int32_t* status_dev, uint32_t limit_us, pa_stream stream) {
+    if (!status_dev) return fail(PA_ERR_INVALID_ARG, "selftest_wait_timeout: status_dev is NULL");
+    if (limit_us == 0 || limit_us > 2000000u)
+        return fail(PA_ERR_INVALID_ARG, "selftest_wait_timeout: limit_us must be in 1 .. 2000000");
+    cudaError_t e = pa::launch_wait_timeout_probe(status_dev, (uint64_t)limit_us * 1000ull,
+                                                  (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "selftest_wait_timeout launch");
+    return ok();
+}
+
 pa_status pa_set_kernel_events(void* start_event, void* stop_event) {
     if ((start_event == nullptr) != (stop_event == nullptr))
         return fail(PA_ERR_INVALID_ARG, "set_kernel_events: give both events or neither");
@@ -562,7 +684,7 @@ pa_status pa_alloc_append(pa_alloc* a, int32_t seq_id, int32_t* slot_out) {
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_append: unknown seq %d", seq_id);
     pa_alloc::Seq& s = it->second;
-    if (s.len % a->block_size == 0) {
+    if ((size_t)(s.len / a->block_size) >= s.blocks.size()) {   // no block (reserved) yet
         if (a->free_list.empty()) return fail(PA_ERR_NO_BLOCKS, "alloc_append: no free block");
         s.blocks.push_back(a->free_list.back());
         a->free_list.pop_back();
@@ -584,7 +706,7 @@ pa_status pa_alloc_append_batch(pa_alloc* a, const int32_t* seq_ids, int32_t n, 
             return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: unknown seq %d", seq_ids[i]);
         if (!seen.insert(seq_ids[i]).second)
             return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: seq %d listed twice", seq_ids[i]);
-        if (it->second.len % a->block_size == 0) ++need;
+        if ((size_t)(it->second.len / a->block_size) >= it->second.blocks.size()) ++need;
     }
     if (need > (int64_t)a->free_list.size())
         return fail(PA_ERR_NO_BLOCKS, "alloc_append_batch: need %lld blocks, %zu free",
@@ -592,6 +714,33 @@ pa_status pa_alloc_append_batch(pa_alloc* a, const int32_t* seq_ids, int32_t n, 
     for (int32_t i = 0; i < n; ++i) {
         pa_status st = pa_alloc_append(a, seq_ids[i], &slots_out[i]);
         if (st != PA_OK) return st;
+    }
+    return ok();
+}
+
+pa_status pa_alloc_reserve_batch(pa_alloc* a, const int32_t* seq_ids, int32_t n,
+                                 int32_t extra_tokens) {
+    if (!a || n < 0 || extra_tokens < 0 || (n > 0 && !seq_ids))
+        return fail(PA_ERR_INVALID_ARG, "alloc_reserve_batch: bad args");
+    int64_t need = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end())
+            return fail(PA_ERR_INVALID_ARG, "alloc_reserve_batch: unknown seq %d", seq_ids[i]);
+        const int64_t want =
+            ((int64_t)it->second.len + extra_tokens + a->block_size - 1) / a->block_size;
+        need += std::max<int64_t>(0, want - (int64_t)it->second.blocks.size());
+    }
+    if (need > (int64_t)a->free_list.size())
+        return fail(PA_ERR_NO_BLOCKS, "alloc_reserve_batch: need %lld blocks, %zu free",
+                    (long long)need, a->free_list.size());
+    for (int32_t i = 0; i < n; ++i) {
+        pa_alloc::Seq& s = a->seqs[seq_ids[i]];
+        const int64_t want = ((int64_t)s.len + extra_tokens + a->block_size - 1) / a->block_size;
+        while ((int64_t)s.blocks.size() < want) {
+            s.blocks.push_back(a->free_list.back());
+            a->free_list.pop_back();
+        }
     }
     return ok();
 }

@@ -72,6 +72,14 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                                      int32_t head_size, int32_t block_size, int32_t num_blocks,
                                      int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_advance_step(int32_t* context_lens, int32_t* slot_mapping,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                int32_t num_seqs, int32_t block_size, int32_t num_blocks,
+                                int64_t* input_positions, int64_t* input_tokens,
+                                const int64_t* sampled_token_ids, int32_t* status,
+                                cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
 // Records `message` as this thread's pa_last_error() text and returns `status`.
 int32_t set_last_error(int32_t status, const char* message);
 

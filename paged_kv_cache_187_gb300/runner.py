@@ -145,3 +145,68 @@ class DecodeRunner:
 
     def seq_tokens(self) -> int:
         return int(self.context_lens.astype(np.int64).sum())
+
+    # ------------------------------------------------------------------ multi-step loop
+    def setup_multistep(self, k: int):
+        """Host side of a k-step decode loop run entirely on the device ("[core] Multi Step
+        Scheduling #7000": k decode steps between scheduler visits, metadata advanced on
+        the GPU).  Reserves every block the loop will touch, builds the block tables once,
+        and stages k steps of q / k / v inputs; the device lengths start at the pre-loop
+        values and pa_advance_step moves them one token per step."""
+        w = self.w
+        S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
+        ids = self.seq_ids
+        self.alloc.pa_alloc_reserve_batch(ids, k)
+        self.ms_k = k
+        self.ms_lens0 = self.alloc.pa_alloc_context_lens(ids)
+        self.block_tables = self.alloc.pa_alloc_block_tables(ids, self.max_blocks)
+        self.block_tables_d = torch.from_numpy(self.block_tables).to(self.device)
+        self.ms_lens0_d = torch.from_numpy(self.ms_lens0).to(self.device)
+        self.context_lens_d = self.ms_lens0_d.clone()
+        self.slots_d = torch.empty(S, dtype=torch.int32, device=self.device)
+        self.ms_max_context_len = int(self.ms_lens0.max()) + k
+        base = self.step_index + 1
+        self.ms_q = [W.randn_16bit((S, Hq, D), w.dtype, W.stream_seed(w, "q", base + j, self.rank),
+                                   self.device) for j in range(k)]
+        self.ms_k_new = [W.randn_16bit((S, Hkv, D), w.dtype,
+                                       W.stream_seed(w, "k_new", base + j, self.rank), self.device)
+                         for j in range(k)]
+        self.ms_v_new = [W.randn_16bit((S, Hkv, D), w.dtype,
+                                       W.stream_seed(w, "v_new", base + j, self.rank), self.device)
+                         for j in range(k)]
+        self.ms_out = [torch.empty((S, Hq, D), dtype=self.tdtype, device=self.device)
+                       for _ in range(k)]
+        need = B.pa_decode_auto_workspace_size(S, Hq, Hkv, D, w.block_size,
+                                               self.ms_max_context_len)
+        if need > self.workspace.numel():
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self
+
+    def run_multistep(self, stream=None, on_step=None):
+        """The k-step loop on the device: per step pa_advance_step (lengths and slots move
+        one token), then pa_decode_step (reshape_and_cache + decode).  Starts from the
+        pre-loop lengths every time, so it can be captured once and replayed."""
+        w = self.w
+        self.context_lens_d.copy_(self.ms_lens0_d)
+        for j in range(self.ms_k):
+            B.pa_advance_step(self.context_lens_d, self.slots_d, self.block_tables_d,
+                              w.block_size, self.num_blocks, status=self.status, stream=stream)
+            B.pa_decode_step(self.ms_out[j], self.ms_q[j], self.ms_k_new[j], self.ms_v_new[j],
+                             self.key_cache, self.value_cache, self.slots_d, self.block_tables_d,
+                             self.context_lens_d, self.ms_max_context_len, w.scale,
+                             workspace=self.workspace, status=self.status, stream=stream)
+            if on_step is not None:
+                on_step(j)
+
+    def capture_multistep(self):
+        """CUDA graph of run_multistep (call run_multistep once before, so that every
+        kernel is loaded and configured outside the capture)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run_multistep()
+        return g
+
+    def finish_multistep(self):
+        """Brings the host allocator to the state after the loop (k appends per sequence,
+        on the reserved blocks) and returns the slots it assigns per step, [k][S]."""
+        return np.stack([self.alloc.pa_alloc_append_batch(self.seq_ids) for _ in range(self.ms_k)])

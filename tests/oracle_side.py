@@ -38,13 +38,18 @@ def record_step(r) -> StepRecord:
 class OracleState:
     """Oracle allocator + (optionally compacted) oracle pools for a runner's workload."""
 
-    def __init__(self, r, steps: list[StepRecord], seqs=None):
+    def __init__(self, r, steps: list[StepRecord], seqs=None, reserve: int = 0):
+        """`reserve` > 0 replays a multi-step loop whose blocks were reserved up front
+        (the allocator's reserve, then one append per sequence per step)."""
         w = r.w
         self.w = w
         S, bs = w.num_seqs, w.block_size
         self.alloc = oracle.Alloc(r.num_blocks, bs, r.alloc_seed, max_seqs=max(S, 1))
         for s in range(S):
             self.alloc.add_seq(s, int(r.prefill_lens[s]))
+        if reserve:
+            for s in range(S):
+                self.alloc.reserve(s, reserve)
         self.prefill_slots = np.concatenate(
             [self.alloc.slots(s, 0, int(r.prefill_lens[s])) for s in range(S)] +
             [np.zeros(0, np.int32)])

@@ -102,3 +102,28 @@ def test_allocator_errors_and_all_or_nothing_batch(pa):
         prod.pa_alloc_append(42)                    # unknown id
     slots = prod.pa_alloc_append_batch([2])
     assert slots.shape == (1,) and slots[0] % 8 == 1
+
+
+def test_reserve_matches_oracle_and_appends_use_reserved_blocks(pa):
+    NB, bs = 64, 16
+    prod = pa.PagedAllocator(NB, bs, 42)
+    ref = oracle.Alloc(NB, bs, 42)
+    lens = [15, 16, 1, 40]
+    for s, L in enumerate(lens):
+        prod.pa_alloc_add_seq(s, L)
+        ref.add_seq(s, L)
+    ids = np.arange(4)
+    prod.pa_alloc_reserve_batch(ids, 8)
+    for s in ids:
+        ref.reserve(int(s), 8)
+    free_after_reserve = prod.num_free
+    assert free_after_reserve == ref.num_free
+    assert np.array_equal(prod.pa_alloc_block_tables(ids, 4), ref.block_tables(ids, 4))
+    for _ in range(8):
+        a = prod.pa_alloc_append_batch(ids)
+        b = np.array([ref.append(int(s)) for s in ids], np.int32)
+        assert np.array_equal(a, b)
+    assert prod.num_free == free_after_reserve          # no pops inside the reservation
+    with pytest.raises(pa.PANoBlocks):
+        prod.pa_alloc_reserve_batch(ids, 10_000)        # all or nothing
+    assert prod.num_free == free_after_reserve

@@ -343,3 +343,23 @@ def test_kv_bytes_per_token_matches_the_quoted_llama13b_figure():
     per_seq = per_token_layer * vals["layers"] * vals["max_context"]
     assert per_token_layer == 20480
     assert abs(per_seq - vals["quoted_bytes_per_sequence"]) / vals["quoted_bytes_per_sequence"] < 0.02
+
+
+def test_allocator_reserve_then_appends_pop_nothing():
+    bs = 8
+    al = oracle.Alloc(20, bs, seed=3)
+    al.add_seq(0, 7)                                     # 1 block
+    al.reserve(0, 10)                                    # 7 + 10 = 17 tokens -> 3 blocks
+    assert al.num_free == 17
+    table = al.block_tables([0], 3)[0]
+    assert (table >= 0).all()
+    for i in range(10):                                  # positions 7 .. 16
+        slot = al.append(0)
+        pos = 7 + i
+        assert slot == table[pos // bs] * bs + pos % bs
+    assert al.num_free == 17
+    al.append(0)                                         # position 17: still block 2
+    assert al.num_free == 17
+    for _ in range(7):                                   # positions 18 .. 24 -> block 3 popped
+        al.append(0)
+    assert al.num_free == 16
