@@ -250,6 +250,19 @@ pa_status pa_advance_step(int32_t* context_lens, int32_t* slot_mapping, const in
                           int32_t num_blocks, int64_t* input_positions, int64_t* input_tokens,
                           const int64_t* sampled_token_ids, int32_t* status_dev, pa_stream stream);
 
+/* Copies whole blocks of both pools on the device, for copy-on-write of shared blocks
+ * ([TALK]: blocks shared between requests, prefix caching): for each pair i, block
+ * block_pairs[2i+1] of key_cache and value_cache takes the contents of block
+ * block_pairs[2i] (every kv head and row; a bit-exact copy).  block_pairs is a device
+ * int32 array [num_pairs][2], e.g. the pairs pa_alloc_take_copies returned, copied to
+ * the device; run it before reshape_and_cache writes into the new blocks.  Pairs
+ * outside the pool are skipped and flagged PA_DEVERR_BAD_BLOCK; a block that is both a
+ * source and a destination in one call races. */
+pa_status pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* block_pairs,
+                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_size,
+                         int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                         int32_t* status_dev, pa_stream stream);
+
 /* Self-test of the failure path: launches a one-warp kernel that waits on a pipeline
  * barrier nobody arrives on, gives up after limit_us (1 .. 2,000,000) microseconds and
  * ORs PA_DEVERR_TIMEOUT into *status_dev, exactly as the decode kernel does when a copy
@@ -291,7 +304,26 @@ pa_status pa_alloc_append_batch(pa_alloc* alloc, const int32_t* seq_ids, int32_t
  * not change, and later appends use the reserved blocks first.  All or nothing. */
 pa_status pa_alloc_reserve_batch(pa_alloc* alloc, const int32_t* seq_ids, int32_t n,
                                  int32_t extra_tokens);
-/* Returns seq_id's blocks to the free list and forgets the sequence. */
+/* Shared prefixes: sequence dst_seq (not live) becomes live with the first num_tokens
+ * tokens of src_seq (<= its length), sharing src_seq's first ceil(num_tokens /
+ * block_size) blocks; each shared block's reference count goes up by one and nothing
+ * is popped.  Before any later append or reserve writes into a block whose count is
+ * above one, the allocator gives the writer a private copy: it pops a new block, puts
+ * it in the writer's table and records the pair (old, new); take those pairs with
+ * pa_alloc_take_copies and copy them with pa_copy_blocks before the step's
+ * reshape_and_cache. */
+pa_status pa_alloc_fork(pa_alloc* alloc, int32_t src_seq, int32_t dst_seq, int32_t num_tokens);
+/* Copy-on-write pairs recorded since the last take. */
+int32_t pa_alloc_num_pending_copies(const pa_alloc* alloc);
+/* Writes the pending (old, new) pairs, in the order recorded, to pairs_out
+ * [max_pairs][2] and clears them; *n_out = their number.  If they do not all fit,
+ * nothing is taken and PA_ERR_INVALID_ARG is returned with *n_out set. */
+pa_status pa_alloc_take_copies(pa_alloc* alloc, int32_t* pairs_out, int32_t max_pairs,
+                               int32_t* n_out);
+/* Reference count of a physical block (0 = free), -1 for an id outside the pool. */
+int32_t pa_alloc_refcount(const pa_alloc* alloc, int32_t block);
+/* Drops seq_id's reference to each of its blocks (blocks no longer referenced return
+ * to the free list, in logical order) and forgets the sequence. */
 pa_status pa_alloc_free_seq(pa_alloc* alloc, int32_t seq_id);
 /* Slots of positions [start, start + n) of seq_id. */
 pa_status pa_alloc_slots(const pa_alloc* alloc, int32_t seq_id, int32_t start, int32_t n,

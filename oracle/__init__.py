@@ -99,6 +99,14 @@ def _load():
         lib.or_alloc_append.restype = i32
         lib.or_alloc_reserve.argtypes = [P, i32, i32]
         lib.or_alloc_reserve.restype = i32
+        lib.or_alloc_fork.argtypes = [P, i32, i32, i32]
+        lib.or_alloc_fork.restype = i32
+        lib.or_alloc_take_copies.argtypes = [P, P, i32]
+        lib.or_alloc_take_copies.restype = i32
+        lib.or_alloc_refcount.argtypes = [P, i32]
+        lib.or_alloc_refcount.restype = i32
+        lib.or_copy_blocks.argtypes = [P, P, P, i32, i32, i32, i32, i32]
+        lib.or_copy_blocks.restype = i32
         lib.or_alloc_free_seq.argtypes = [P, i32]
         lib.or_alloc_free_seq.restype = i32
         lib.or_alloc_slots.argtypes = [P, i32, i32, i32, P]
@@ -162,6 +170,15 @@ def reshape_and_cache(key_bits, value_bits, key_cache_bits, value_cache_bits, sl
     return int(lib.or_reshape_and_cache(_ptr(k), _ptr(v), _ptr(key_cache_bits),
                                         _ptr(value_cache_bits), _ptr(sm), T, Hkv, D,
                                         block_size, NB))
+
+
+def copy_blocks(key_cache_bits, value_cache_bits, pairs) -> int:
+    """Copy whole blocks old -> new for each (old, new) row of pairs, in place."""
+    lib = _load()
+    pr = _c(pairs, np.int32).reshape(-1, 2)
+    NB, Hkv, bs, D = key_cache_bits.shape
+    return int(lib.or_copy_blocks(_ptr(key_cache_bits), _ptr(value_cache_bits), _ptr(pr),
+                                  pr.shape[0], Hkv, D, bs, NB))
 
 
 # --------------------------------------------------------------------------- decode
@@ -251,6 +268,20 @@ class Alloc:
 
     def reserve(self, seq_id: int, extra_tokens: int):
         self._chk(self._lib.or_alloc_reserve(self._h, seq_id, extra_tokens))
+
+    def fork(self, src: int, dst: int, num_tokens: int):
+        self._chk(self._lib.or_alloc_fork(self._h, src, dst, num_tokens))
+
+    def take_copies(self) -> np.ndarray:
+        """Pending copy-on-write pairs [n, 2] (old, new), cleared."""
+        n = self._lib.or_alloc_take_copies(self._h, None, 0)
+        out = np.zeros((max(n, 1), 2), dtype=np.int32)
+        got = self._lib.or_alloc_take_copies(self._h, _ptr(out), n)
+        assert got == n
+        return out[:n]
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.or_alloc_refcount(self._h, block))
 
     def free_seq(self, seq_id: int):
         self._chk(self._lib.or_alloc_free_seq(self._h, seq_id))

@@ -332,7 +332,8 @@ int32_t or_paged_decode_v2(double* out, const uint16_t* q, const uint16_t* k_cac
 /*  4. append(id) pops one block first when position len has no block yet      */
 /*     (len a multiple of block_size, nothing reserved ahead), then returns the */
 /*     slot of position len and increments len.                                 */
-/*  5. free_seq(id) pushes the sequence's blocks back in logical order.         */
+/*  5. free_seq(id) pushes the sequence's blocks back in logical order (with   */
+/*     sharing: only the blocks whose reference count drops to 0).              */
 /*  6. A request that needs more blocks than are free fails and changes         */
 /*     nothing.                                                                */
 /* ------------------------------------------------------------------------- */
@@ -347,10 +348,26 @@ uint64_t or_splitmix64_next(uint64_t* state) {
     return z ^ (z >> 31);
 }
 
+/* Shared prefixes ([TALK]: space sharing between requests, prefix caching).  Spec:
+ *  7. Every block has a reference count: the live sequences whose table holds it.
+ *     A popped block starts at 1.
+ *  8. fork(src, dst, n): dst becomes live with length n <= len(src) and the first
+ *     ceil(n / block_size) blocks of src, each count + 1; nothing is popped.
+ *  9. Copy-on-write: when append (or reserve, see below) is about to write position
+ *     len into a block whose count is > 1, it first pops a new block, records the
+ *     pair (old, new) in the pending-copy list, puts the new block in the table in
+ *     place of the old one and decrements the old one's count.  reserve(id, extra),
+ *     extra > 0, does this to the block of position len before popping, so that a
+ *     loop advanced on the device never writes into a shared block.
+ * 10. take_copies returns the pending pairs in the order recorded and clears them;
+ *     the caller copies those blocks on the device before writing new rows. */
 typedef struct {
     int32_t num_blocks, block_size, max_seqs;
     int32_t* free_list;
     int32_t num_free;
+    int32_t* refcount;     /* per physical block */
+    int32_t* copies;       /* pending copy-on-write pairs (old, new) */
+    int32_t ncopies, copies_cap;
     int32_t** blocks;      /* per sequence id: its physical blocks in logical order */
     int32_t* nblocks;
     int32_t* cap;
@@ -375,6 +392,7 @@ or_alloc* or_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed,
         a->free_list[j] = tmp;
     }
     a->num_free = num_blocks;
+    a->refcount = (int32_t*)calloc((size_t)num_blocks, sizeof(int32_t));
     a->blocks = (int32_t**)calloc((size_t)max_seqs, sizeof(int32_t*));
     a->nblocks = (int32_t*)calloc((size_t)max_seqs, sizeof(int32_t));
     a->cap = (int32_t*)calloc((size_t)max_seqs, sizeof(int32_t));
@@ -387,7 +405,7 @@ void or_alloc_destroy(or_alloc* a) {
     if (!a) return;
     for (int32_t i = 0; i < a->max_seqs; ++i) free(a->blocks[i]);
     free(a->blocks); free(a->nblocks); free(a->cap); free(a->len); free(a->live);
-    free(a->free_list);
+    free(a->free_list); free(a->refcount); free(a->copies);
     free(a);
 }
 
@@ -401,6 +419,34 @@ static void push_block(or_alloc* a, int32_t id, int32_t phys) {
     a->blocks[id][a->nblocks[id]++] = phys;
 }
 
+/* Pops the next free block for sequence id (reference count 1). */
+static int32_t pop_block(or_alloc* a) {
+    int32_t b = a->free_list[--a->num_free];
+    a->refcount[b] = 1;
+    return b;
+}
+
+/* Would writing position len of id hit a shared block (rule 9)? */
+static int needs_cow(const or_alloc* a, int32_t id) {
+    int32_t L = a->len[id];
+    int32_t logical = L / a->block_size;
+    return logical < a->nblocks[id] && a->refcount[a->blocks[id][logical]] > 1;
+}
+
+static void copy_on_write(or_alloc* a, int32_t id) {
+    int32_t logical = a->len[id] / a->block_size;
+    int32_t old = a->blocks[id][logical];
+    int32_t fresh = pop_block(a);
+    a->refcount[old] -= 1;
+    a->blocks[id][logical] = fresh;
+    if (a->ncopies + 2 > a->copies_cap) {
+        a->copies_cap = a->copies_cap ? 2 * a->copies_cap : 16;
+        a->copies = (int32_t*)realloc(a->copies, sizeof(int32_t) * (size_t)a->copies_cap);
+    }
+    a->copies[a->ncopies++] = old;
+    a->copies[a->ncopies++] = fresh;
+}
+
 /* Returns 0, -1 (bad id or already live), -3 (not enough free blocks). */
 int32_t or_alloc_add_seq(or_alloc* a, int32_t id, int32_t num_tokens) {
     if (id < 0 || id >= a->max_seqs || a->live[id] || num_tokens < 0) return -1;
@@ -409,7 +455,7 @@ int32_t or_alloc_add_seq(or_alloc* a, int32_t id, int32_t num_tokens) {
     a->live[id] = 1;
     a->nblocks[id] = 0;
     a->len[id] = num_tokens;
-    for (int32_t i = 0; i < need; ++i) push_block(a, id, a->free_list[--a->num_free]);
+    for (int32_t i = 0; i < need; ++i) push_block(a, id, pop_block(a));
     return 0;
 }
 
@@ -419,7 +465,10 @@ int32_t or_alloc_append(or_alloc* a, int32_t id, int32_t* slot) {
     int32_t L = a->len[id];
     if (L / a->block_size >= a->nblocks[id]) {   /* position L needs a block not yet owned */
         if (a->num_free == 0) return -3;
-        push_block(a, id, a->free_list[--a->num_free]);
+        push_block(a, id, pop_block(a));
+    } else if (needs_cow(a, id)) {               /* position L is in a shared block */
+        if (a->num_free == 0) return -3;
+        copy_on_write(a, id);
     }
     *slot = a->blocks[id][L / a->block_size] * a->block_size + L % a->block_size;
     a->len[id] = L + 1;
@@ -435,15 +484,68 @@ int32_t or_alloc_reserve(or_alloc* a, int32_t id, int32_t extra) {
     if (id < 0 || id >= a->max_seqs || !a->live[id] || extra < 0) return -1;
     int32_t want = (a->len[id] + extra + a->block_size - 1) / a->block_size;
     int32_t need = want - a->nblocks[id];
-    if (need <= 0) return 0;
-    if (need > a->num_free) return -3;
-    for (int32_t i = 0; i < need; ++i) push_block(a, id, a->free_list[--a->num_free]);
+    int32_t cow = (extra > 0 && needs_cow(a, id)) ? 1 : 0;
+    if ((need > 0 ? need : 0) + cow > a->num_free) return -3;
+    if (cow) copy_on_write(a, id);
+    for (int32_t i = 0; i < need; ++i) push_block(a, id, pop_block(a));
     return 0;
+}
+
+/* Rule 8.  Returns 0, -1 (bad ids, dst live, src not live, n > len(src)). */
+int32_t or_alloc_fork(or_alloc* a, int32_t src, int32_t dst, int32_t num_tokens) {
+    if (src < 0 || src >= a->max_seqs || !a->live[src]) return -1;
+    if (dst < 0 || dst >= a->max_seqs || a->live[dst] || num_tokens < 0) return -1;
+    if (num_tokens > a->len[src]) return -1;
+    int32_t nb = (num_tokens + a->block_size - 1) / a->block_size;
+    a->live[dst] = 1;
+    a->nblocks[dst] = 0;
+    a->len[dst] = num_tokens;
+    for (int32_t i = 0; i < nb; ++i) {
+        int32_t b = a->blocks[src][i];
+        a->refcount[b] += 1;
+        push_block(a, dst, b);
+    }
+    return 0;
+}
+
+/* Rule 10.  Writes up to max_pairs (old, new) pairs; returns the number of pending
+ * pairs, and takes (clears) them only if they all fit. */
+int32_t or_alloc_take_copies(or_alloc* a, int32_t* pairs, int32_t max_pairs) {
+    int32_t n = a->ncopies / 2;
+    if (n > max_pairs) return n;
+    for (int32_t i = 0; i < 2 * n; ++i) pairs[i] = a->copies[i];
+    a->ncopies = 0;
+    return n;
+}
+
+int32_t or_alloc_refcount(const or_alloc* a, int32_t block) {
+    return (block >= 0 && block < a->num_blocks) ? a->refcount[block] : -1;
+}
+
+/* Copies whole blocks (every kv head, every row) of both pools: for each pair,
+ * block `new` takes the contents of block `old`.  Bit-exact. */
+int32_t or_copy_blocks(uint16_t* key_cache, uint16_t* value_cache, const int32_t* pairs,
+                       int32_t n, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                       int32_t num_blocks) {
+    int64_t per = (int64_t)num_kv_heads * block_size * head_size;
+    int32_t bad = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t from = pairs[2 * i], to = pairs[2 * i + 1];
+        if (from < 0 || from >= num_blocks || to < 0 || to >= num_blocks) { ++bad; continue; }
+        for (int64_t e = 0; e < per; ++e) {
+            key_cache[to * per + e] = key_cache[from * per + e];
+            value_cache[to * per + e] = value_cache[from * per + e];
+        }
+    }
+    return bad;
 }
 
 int32_t or_alloc_free_seq(or_alloc* a, int32_t id) {
     if (id < 0 || id >= a->max_seqs || !a->live[id]) return -1;
-    for (int32_t i = 0; i < a->nblocks[id]; ++i) a->free_list[a->num_free++] = a->blocks[id][i];
+    for (int32_t i = 0; i < a->nblocks[id]; ++i) {
+        int32_t b = a->blocks[id][i];
+        if (--a->refcount[b] == 0) a->free_list[a->num_free++] = b;
+    }
     a->nblocks[id] = 0;
     a->len[id] = 0;
     a->live[id] = 0;

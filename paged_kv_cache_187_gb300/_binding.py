@@ -84,6 +84,11 @@ def _load():
         "pa_alloc_append_batch": ([P, P, i32, P], i32),
         "pa_alloc_free_seq": ([P, i32], i32),
         "pa_alloc_reserve_batch": ([P, P, i32, i32], i32),
+        "pa_alloc_fork": ([P, i32, i32, i32], i32),
+        "pa_alloc_num_pending_copies": ([P], i32),
+        "pa_alloc_take_copies": ([P, P, i32, ctypes.POINTER(i32)], i32),
+        "pa_alloc_refcount": ([P, i32], i32),
+        "pa_copy_blocks": ([P, P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
         "pa_advance_step": ([P, P, P, i32, i32, i32, i32, P, P, P, P, P], i32),
         "pa_alloc_slots": ([P, i32, i32, i32, P], i32),
         "pa_alloc_block_tables": ([P, P, i32, i32, P], i32),
@@ -355,6 +360,19 @@ def pa_advance_step(context_lens, slot_mapping, block_tables, block_size: int, n
         _opt_dev(status, "status"), _stream(stream)))
 
 
+def pa_copy_blocks(key_cache, value_cache, block_pairs, status=None, stream=None):
+    """Device copy of whole blocks old -> new for each row (old, new) of block_pairs
+    (int32 [n, 2] on the device), in both pools."""
+    import torch
+    NB, Hkv, bs, D = key_cache.shape
+    if value_cache.shape != key_cache.shape or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("copy_blocks: pools [NB, Hkv, bs, D] and pairs [n, 2] expected")
+    _check(_lib.pa_copy_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+                               _dev(block_pairs, "block_pairs", torch.int32),
+                               int(block_pairs.shape[0]), Hkv, D, bs, NB, _dt(key_cache),
+                               _opt_dev(status, "status"), _stream(stream)))
+
+
 def pa_selftest_wait_timeout(status, limit_us: int, stream=None):
     """Runs the bounded-wait self-test kernel; sets PA_DEVERR_TIMEOUT in `status`."""
     import torch
@@ -426,6 +444,20 @@ class PagedAllocator:
     def pa_alloc_reserve_batch(self, seq_ids, extra_tokens: int):
         ids = _np_i32(seq_ids)
         _check(_lib.pa_alloc_reserve_batch(self._h, _nptr(ids), ids.size, int(extra_tokens)))
+
+    def pa_alloc_fork(self, src_seq: int, dst_seq: int, num_tokens: int):
+        _check(_lib.pa_alloc_fork(self._h, int(src_seq), int(dst_seq), int(num_tokens)))
+
+    def pa_alloc_take_copies(self) -> np.ndarray:
+        """Pending copy-on-write pairs [n, 2] (old, new), cleared."""
+        n = int(_lib.pa_alloc_num_pending_copies(self._h))
+        out = np.zeros((max(n, 1), 2), dtype=np.int32)
+        got = ctypes.c_int32(0)
+        _check(_lib.pa_alloc_take_copies(self._h, _nptr(out), n, ctypes.byref(got)))
+        return out[:got.value]
+
+    def pa_alloc_refcount(self, block: int) -> int:
+        return int(_lib.pa_alloc_refcount(self._h, int(block)))
 
     def pa_alloc_free_seq(self, seq_id: int):
         _check(_lib.pa_alloc_free_seq(self._h, int(seq_id)))

@@ -27,6 +27,7 @@ SOURCES = [
     "pa_aux.cu",
     "pa_noalloc.cu",
     "pa_host.cpp",
+    "pa_alloc.cpp",
 ]
 
 

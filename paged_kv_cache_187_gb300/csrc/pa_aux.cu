@@ -5,6 +5,7 @@
 //   * plan: lists the V2 partitions of every sequence ("vLLM Project Update" talk, the V2
 //     kernel that partitions sequences and spreads them over SMs) in claim order and
 //     resets the counters the decode kernel uses.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -234,6 +235,31 @@ __global__ void __launch_bounds__(256)
     slot_mapping[s] = slot;
 }
 
+// Copy-on-write of shared blocks ("vLLM Project Update" talk: blocks shared between
+// requests, prefix caching): for each (old, new) pair, block `new` of both pools takes
+// the contents of block `old` -- every kv head and row, 16 bytes per thread-step.
+// Pairs outside the pool are skipped and flagged PA_DEVERR_BAD_BLOCK.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                       const int32_t* __restrict__ pairs, int64_t vecs_per_block, int32_t num_blocks,
+                       int32_t* status) {
+    const int32_t i = blockIdx.x;
+    const int32_t from = pairs[2 * i], to = pairs[2 * i + 1];
+    if (from < 0 || from >= num_blocks || to < 0 || to >= num_blocks) {
+        if (threadIdx.x == 0 && status) atomicOr(status, 2 /* PA_DEVERR_BAD_BLOCK */);
+        return;
+    }
+    const uint4* ks = key_cache + (int64_t)from * vecs_per_block;
+    const uint4* vs = value_cache + (int64_t)from * vecs_per_block;
+    uint4* kd = key_cache + (int64_t)to * vecs_per_block;
+    uint4* vd = value_cache + (int64_t)to * vecs_per_block;
+    for (int64_t e = threadIdx.x + (int64_t)blockIdx.y * blockDim.x; e < vecs_per_block;
+         e += (int64_t)gridDim.y * blockDim.x) {
+        kd[e] = ks[e];
+        vd[e] = vs[e];
+    }
+}
+
 // Exercises the bounded pipeline wait: waits on a shared-memory barrier that nothing
 // will ever arrive on, gives up after limit_ns, and reports PA_DEVERR_TIMEOUT exactly as
 // the decode kernel does when a TMA completion never comes.
@@ -260,6 +286,18 @@ cudaError_t launch_advance_step(int32_t* context_lens, int32_t* slot_mapping,
     advance_step_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
         context_lens, slot_mapping, block_tables, max_blocks_per_seq, num_seqs, block_size,
         num_blocks, input_positions, input_tokens, sampled_token_ids, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* key_cache, void* value_cache, const int32_t* pairs,
+                               int32_t num_pairs, int64_t bytes_per_block, int32_t num_blocks,
+                               int32_t* status, cudaStream_t stream) {
+    if (num_pairs <= 0) return cudaSuccess;
+    const int64_t vecs = bytes_per_block / 16;
+    const int32_t ys = (int32_t)std::min<int64_t>(8, (vecs + 255) / 256);
+    copy_blocks_kernel<<<dim3(num_pairs, ys), 256, 0, stream>>>(
+        static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), pairs, vecs, num_blocks,
+        status);
     return cudaGetLastError();
 }
 

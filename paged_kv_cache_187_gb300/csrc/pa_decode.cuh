@@ -312,14 +312,15 @@ struct MmaConsumer {
                                          float scale_log2, int lane, float (*)[BS]) {
         const int r8 = lane & 7, mi = lane >> 3;
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-        // S^T[token][head] = K Q^T
-        float sc[MT][NT][4];
+        // S^T[token][head] = K Q^T, the head-dim steps split over two accumulator chains
+        // (even and odd steps) so that consecutive mma.sync do not wait on each other
+        float sc[MT][NT][4], sc2[MT][NT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) sc[mt][nt][r] = 0.f;
+                for (int r = 0; r < 4; ++r) sc[mt][nt][r] = sc2[mt][nt][r] = 0.f;
 #pragma unroll
         for (int i = 0; i < KS; ++i) {
 #pragma unroll
@@ -328,12 +329,22 @@ struct MmaConsumer {
                 const int t = mt * 16 + r8 + 8 * (mi & 1);
                 ldmatrix_x4(a, kbase + swz<C>(t, 2 * i + (mi >> 1)));
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_16816<C::kBf16>(sc[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (i & 1) mma_16816<C::kBf16>(sc2[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                    else mma_16816<C::kBf16>(sc[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                }
             }
         }
-        // online softmax, per query head (columns 2*(lane&3) and +1 of each n-tile)
-        uint32_t pb[MT][NT][2];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sc[mt][nt][r] += sc2[mt][nt][r];
+        // online softmax, per query head (columns 2*(lane&3) and +1 of each n-tile).  The
+        // weights enter the PV product as two 16-bit terms, P = P_hi + P_lo, so that their
+        // rounding to the operand type costs ~2^-17 instead of 2^-9 (bf16) of relative error.
+        uint32_t pb[MT][NT][2], pl[MT][NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             float mx[2] = {-INFINITY, -INFINITY};
@@ -366,8 +377,15 @@ struct MmaConsumer {
                     sc[mt][nt][r] = e;
                     ps[r & 1] += e;
                 }
-                pb[mt][nt][0] = movmatrix_trans(pack2<C::kBf16>(sc[mt][nt][0], sc[mt][nt][1]));
-                pb[mt][nt][1] = movmatrix_trans(pack2<C::kBf16>(sc[mt][nt][2], sc[mt][nt][3]));
+                const uint32_t h01 = pack2<C::kBf16>(sc[mt][nt][0], sc[mt][nt][1]);
+                const uint32_t h23 = pack2<C::kBf16>(sc[mt][nt][2], sc[mt][nt][3]);
+                float r0, r1, r2, r3;
+                unpack2<C::kBf16>(h01, r0, r1);
+                unpack2<C::kBf16>(h23, r2, r3);
+                pb[mt][nt][0] = movmatrix_trans(h01);
+                pb[mt][nt][1] = movmatrix_trans(h23);
+                pl[mt][nt][0] = movmatrix_trans(pack2<C::kBf16>(sc[mt][nt][0] - r0, sc[mt][nt][1] - r1));
+                pl[mt][nt][1] = movmatrix_trans(pack2<C::kBf16>(sc[mt][nt][2] - r2, sc[mt][nt][3] - r3));
             }
             l[nt][0] = l[nt][0] * alpha[0] + ps[0];
             l[nt][1] = l[nt][1] * alpha[1] + ps[1];
@@ -402,8 +420,10 @@ struct MmaConsumer {
                     a[3] &= lo8 | hi8;
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt) {
                     mma_16816<C::kBf16>(acc[i][nt], a, pb[mt][nt][0], pb[mt][nt][1]);
+                    mma_16816<C::kBf16>(acc[i][nt], a, pl[mt][nt][0], pl[mt][nt][1]);
+                }
             }
         }
     }

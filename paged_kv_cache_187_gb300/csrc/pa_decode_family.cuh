@@ -6,8 +6,10 @@
 
 #include "pa_decode.cuh"
 
+// Tensor-core path: two consumer warps for 16-token blocks (short tiles, more of them);
+// one for 32-token blocks, whose tiles already carry twice the work per wait.
 #ifndef PA_MMA_CONSUMERS
-#define PA_MMA_CONSUMERS 1
+#define PA_MMA_CONSUMERS(BS) ((BS) == 16 ? 2 : 1)
 #endif
 #ifndef PA_CORE_CONSUMERS
 #define PA_CORE_CONSUMERS 2
@@ -27,17 +29,17 @@ constexpr int stages_for() {
 
 // Consumer warps per CTA: the CUDA-core path needs more warps to keep up with HBM than
 // the tensor-core path does.
-template <bool MMA>
+template <bool MMA, int BS>
 constexpr int consumers_for() {
-    return MMA ? PA_MMA_CONSUMERS : PA_CORE_CONSUMERS;
+    return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
 
 template <int D, int BS, bool BF16, bool MMA, int HCAP>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
-    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D, BS, consumers_for<MMA>()>(), 2,
-                        consumers_for<MMA>()>;
+    constexpr int kCons = consumers_for<MMA, BS>();
+    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D, BS, kCons>(), 2, kCons>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
     static bool configured = false;   // per instantiation; attribute setting is idempotent

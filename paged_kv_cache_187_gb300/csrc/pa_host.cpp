@@ -469,6 +469,25 @@ pa_status pa_advance_step(int32_t* context_lens, int32_t* slot_mapping, const in
     return ok();
 }
 
+pa_status pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* block_pairs,
+                         int32_t num_pairs, int32_t num_kv_heads, int32_t head_size,
+                         int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                         int32_t* status_dev, pa_stream stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "copy_blocks: sizes must be positive");
+    if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "copy_blocks: dtype");
+    if (num_pairs == 0) return ok();
+    if (!key_cache || !value_cache || !block_pairs)
+        return fail(PA_ERR_INVALID_ARG, "copy_blocks: null pointer");
+    const int64_t bytes = (int64_t)num_kv_heads * block_size * head_size * 2;
+    if (!aligned16(key_cache) || !aligned16(value_cache) || bytes % 16)
+        return fail(PA_ERR_INVALID_ARG, "copy_blocks: pools must be 16-byte aligned, blocks 16-byte multiples");
+    cudaError_t e = pa::launch_copy_blocks(key_cache, value_cache, block_pairs, num_pairs, bytes,
+                                           num_blocks, status_dev, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+    return ok();
+}
+
 pa_status pa_selftest_wait_timeout(int32_t* status_dev, uint32_t limit_us, pa_stream stream) {
     if (!status_dev) return fail(PA_ERR_INVALID_ARG, "selftest_wait_timeout: status_dev is NULL");
     if (limit_us == 0 || limit_us > 2000000u)
@@ -603,199 +622,6 @@ pa_status pa_decode_step(void* out, const void* query, const void* key, const vo
                           context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                           num_blocks, max_context_len, scale, dtype, workspace, workspace_bytes,
                           status_dev, stream);
-}
-
-}  // extern "C"
-
-// =====================================================================================
-// Host block allocator
-// =====================================================================================
-struct pa_alloc {
-    int32_t num_blocks = 0;
-    int32_t block_size = 0;
-    std::vector<int32_t> free_list;   // popped from the back
-    struct Seq {
-        std::vector<int32_t> blocks;
-        int32_t len = 0;
-    };
-    std::unordered_map<int32_t, Seq> seqs;
-};
-
-namespace {
-
-// splitmix64 (Steele, Lea and Flood, OOPSLA 2014).
-uint64_t splitmix64(uint64_t& s) {
-    s += 0x9E3779B97F4A7C15ull;
-    uint64_t z = s;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
-}
-
-}  // namespace
-
-extern "C" {
-
-pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, uint64_t seed, pa_alloc** out) {
-    if (!out) return fail(PA_ERR_INVALID_ARG, "alloc_create: null output");
-    *out = nullptr;
-    if (num_blocks <= 0 || block_size <= 0)
-        return fail(PA_ERR_INVALID_ARG, "alloc_create: num_blocks and block_size must be positive");
-    if ((int64_t)num_blocks * block_size > INT32_MAX)
-        return fail(PA_ERR_INVALID_ARG, "alloc_create: num_blocks * block_size overflows int32 slots");
-    auto* a = new pa_alloc;
-    a->num_blocks = num_blocks;
-    a->block_size = block_size;
-    a->free_list.resize(num_blocks);
-    for (int32_t i = 0; i < num_blocks; ++i) a->free_list[i] = i;
-    uint64_t st = seed;
-    for (int32_t i = num_blocks - 1; i >= 1; --i) {
-        const int32_t j = (int32_t)(splitmix64(st) % (uint64_t)(i + 1));
-        std::swap(a->free_list[i], a->free_list[j]);
-    }
-    *out = a;
-    return ok();
-}
-
-void pa_alloc_destroy(pa_alloc* a) { delete a; }
-
-int32_t pa_alloc_num_free(const pa_alloc* a) { return a ? (int32_t)a->free_list.size() : 0; }
-
-pa_status pa_alloc_add_seq(pa_alloc* a, int32_t seq_id, int32_t num_tokens) {
-    if (!a || seq_id < 0 || num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "alloc_add_seq: bad args");
-    if (a->seqs.count(seq_id)) return fail(PA_ERR_INVALID_ARG, "alloc_add_seq: seq %d is live", seq_id);
-    const int64_t need = ((int64_t)num_tokens + a->block_size - 1) / a->block_size;
-    if (need > (int64_t)a->free_list.size())
-        return fail(PA_ERR_NO_BLOCKS, "alloc_add_seq: need %lld blocks, %zu free", (long long)need,
-                    a->free_list.size());
-    pa_alloc::Seq s;
-    s.len = num_tokens;
-    s.blocks.reserve(need);
-    for (int64_t i = 0; i < need; ++i) {
-        s.blocks.push_back(a->free_list.back());
-        a->free_list.pop_back();
-    }
-    a->seqs.emplace(seq_id, std::move(s));
-    return ok();
-}
-
-pa_status pa_alloc_append(pa_alloc* a, int32_t seq_id, int32_t* slot_out) {
-    if (!a || !slot_out) return fail(PA_ERR_INVALID_ARG, "alloc_append: null argument");
-    auto it = a->seqs.find(seq_id);
-    if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_append: unknown seq %d", seq_id);
-    pa_alloc::Seq& s = it->second;
-    if ((size_t)(s.len / a->block_size) >= s.blocks.size()) {   // no block (reserved) yet
-        if (a->free_list.empty()) return fail(PA_ERR_NO_BLOCKS, "alloc_append: no free block");
-        s.blocks.push_back(a->free_list.back());
-        a->free_list.pop_back();
-    }
-    *slot_out = s.blocks[s.len / a->block_size] * a->block_size + s.len % a->block_size;
-    s.len += 1;
-    return ok();
-}
-
-pa_status pa_alloc_append_batch(pa_alloc* a, const int32_t* seq_ids, int32_t n, int32_t* slots_out) {
-    if (!a || n < 0 || (n > 0 && (!seq_ids || !slots_out)))
-        return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: bad args");
-    int64_t need = 0;
-    std::unordered_set<int32_t> seen;
-    seen.reserve((size_t)n * 2);
-    for (int32_t i = 0; i < n; ++i) {
-        auto it = a->seqs.find(seq_ids[i]);
-        if (it == a->seqs.end())
-            return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: unknown seq %d", seq_ids[i]);
-        if (!seen.insert(seq_ids[i]).second)
-            return fail(PA_ERR_INVALID_ARG, "alloc_append_batch: seq %d listed twice", seq_ids[i]);
-        if ((size_t)(it->second.len / a->block_size) >= it->second.blocks.size()) ++need;
-    }
-    if (need > (int64_t)a->free_list.size())
-        return fail(PA_ERR_NO_BLOCKS, "alloc_append_batch: need %lld blocks, %zu free",
-                    (long long)need, a->free_list.size());
-    for (int32_t i = 0; i < n; ++i) {
-        pa_status st = pa_alloc_append(a, seq_ids[i], &slots_out[i]);
-        if (st != PA_OK) return st;
-    }
-    return ok();
-}
-
-pa_status pa_alloc_reserve_batch(pa_alloc* a, const int32_t* seq_ids, int32_t n,
-                                 int32_t extra_tokens) {
-    if (!a || n < 0 || extra_tokens < 0 || (n > 0 && !seq_ids))
-        return fail(PA_ERR_INVALID_ARG, "alloc_reserve_batch: bad args");
-    int64_t need = 0;
-    for (int32_t i = 0; i < n; ++i) {
-        auto it = a->seqs.find(seq_ids[i]);
-        if (it == a->seqs.end())
-            return fail(PA_ERR_INVALID_ARG, "alloc_reserve_batch: unknown seq %d", seq_ids[i]);
-        const int64_t want =
-            ((int64_t)it->second.len + extra_tokens + a->block_size - 1) / a->block_size;
-        need += std::max<int64_t>(0, want - (int64_t)it->second.blocks.size());
-    }
-    if (need > (int64_t)a->free_list.size())
-        return fail(PA_ERR_NO_BLOCKS, "alloc_reserve_batch: need %lld blocks, %zu free",
-                    (long long)need, a->free_list.size());
-    for (int32_t i = 0; i < n; ++i) {
-        pa_alloc::Seq& s = a->seqs[seq_ids[i]];
-        const int64_t want = ((int64_t)s.len + extra_tokens + a->block_size - 1) / a->block_size;
-        while ((int64_t)s.blocks.size() < want) {
-            s.blocks.push_back(a->free_list.back());
-            a->free_list.pop_back();
-        }
-    }
-    return ok();
-}
-
-pa_status pa_alloc_free_seq(pa_alloc* a, int32_t seq_id) {
-    if (!a) return fail(PA_ERR_INVALID_ARG, "alloc_free_seq: null handle");
-    auto it = a->seqs.find(seq_id);
-    if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_free_seq: unknown seq %d", seq_id);
-    for (int32_t b : it->second.blocks) a->free_list.push_back(b);
-    a->seqs.erase(it);
-    return ok();
-}
-
-pa_status pa_alloc_slots(const pa_alloc* a, int32_t seq_id, int32_t start, int32_t n, int32_t* out) {
-    if (!a || (n > 0 && !out) || start < 0 || n < 0) return fail(PA_ERR_INVALID_ARG, "alloc_slots: bad args");
-    auto it = a->seqs.find(seq_id);
-    if (it == a->seqs.end()) return fail(PA_ERR_INVALID_ARG, "alloc_slots: unknown seq %d", seq_id);
-    const pa_alloc::Seq& s = it->second;
-    if ((int64_t)start + n > s.len) return fail(PA_ERR_INVALID_ARG, "alloc_slots: past the sequence end");
-    for (int32_t i = 0; i < n; ++i) {
-        const int32_t t = start + i;
-        out[i] = s.blocks[t / a->block_size] * a->block_size + t % a->block_size;
-    }
-    return ok();
-}
-
-pa_status pa_alloc_block_tables(const pa_alloc* a, const int32_t* seq_ids, int32_t n,
-                                int32_t max_blocks_per_seq, int32_t* out) {
-    if (!a || n < 0 || max_blocks_per_seq <= 0 || (n > 0 && (!seq_ids || !out)))
-        return fail(PA_ERR_INVALID_ARG, "alloc_block_tables: bad args");
-    for (int32_t r = 0; r < n; ++r) {
-        auto it = a->seqs.find(seq_ids[r]);
-        if (it == a->seqs.end())
-            return fail(PA_ERR_INVALID_ARG, "alloc_block_tables: unknown seq %d", seq_ids[r]);
-        const std::vector<int32_t>& b = it->second.blocks;
-        if ((int64_t)b.size() > max_blocks_per_seq)
-            return fail(PA_ERR_INVALID_ARG, "alloc_block_tables: seq %d has %zu blocks > %d",
-                        seq_ids[r], b.size(), max_blocks_per_seq);
-        int32_t* row = out + (size_t)r * max_blocks_per_seq;
-        std::copy(b.begin(), b.end(), row);
-        std::fill(row + b.size(), row + max_blocks_per_seq, -1);
-    }
-    return ok();
-}
-
-pa_status pa_alloc_context_lens(const pa_alloc* a, const int32_t* seq_ids, int32_t n, int32_t* out) {
-    if (!a || n < 0 || (n > 0 && (!seq_ids || !out)))
-        return fail(PA_ERR_INVALID_ARG, "alloc_context_lens: bad args");
-    for (int32_t r = 0; r < n; ++r) {
-        auto it = a->seqs.find(seq_ids[r]);
-        if (it == a->seqs.end())
-            return fail(PA_ERR_INVALID_ARG, "alloc_context_lens: unknown seq %d", seq_ids[r]);
-        out[r] = it->second.len;
-    }
-    return ok();
 }
 
 }  // extern "C"

@@ -78,6 +78,9 @@ cudaError_t launch_advance_step(int32_t* context_lens, int32_t* slot_mapping,
                                 int64_t* input_positions, int64_t* input_tokens,
                                 const int64_t* sampled_token_ids, int32_t* status,
                                 cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* key_cache, void* value_cache, const int32_t* pairs,
+                               int32_t num_pairs, int64_t bytes_per_block, int32_t num_blocks,
+                               int32_t* status, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Records `message` as this thread's pa_last_error() text and returns `status`.

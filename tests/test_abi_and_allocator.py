@@ -127,3 +127,69 @@ def test_reserve_matches_oracle_and_appends_use_reserved_blocks(pa):
     with pytest.raises(pa.PANoBlocks):
         prod.pa_alloc_reserve_batch(ids, 10_000)        # all or nothing
     assert prod.num_free == free_after_reserve
+
+
+def test_sharing_allocator_matches_oracle_under_random_requests(pa):
+    rng = np.random.default_rng(77)
+    NB, bs = 200, 16
+    prod = pa.PagedAllocator(NB, bs, 5)
+    ref = oracle.Alloc(NB, bs, 5)
+    live = {}
+    next_id = 0
+    for step in range(600):
+        op = int(rng.integers(0, 5))
+        if op == 0 or not live:                               # new sequence
+            n = int(rng.integers(0, 70))
+            try:
+                prod.pa_alloc_add_seq(next_id, n)
+            except pa.PANoBlocks:
+                with pytest.raises(oracle.OracleAllocError):
+                    ref.add_seq(next_id, n)
+                continue
+            ref.add_seq(next_id, n)
+            live[next_id] = n
+            next_id += 1
+        elif op == 1:                                         # fork a prefix
+            src = int(rng.choice(list(live)))
+            n = int(rng.integers(0, live[src] + 1))
+            prod.pa_alloc_fork(src, next_id, n)
+            ref.fork(src, next_id, n)
+            live[next_id] = n
+            next_id += 1
+        elif op == 2:                                         # append to some sequences
+            ids = rng.choice(list(live), size=min(len(live), 4), replace=False).astype(np.int32)
+            try:
+                a = prod.pa_alloc_append_batch(ids)
+            except pa.PANoBlocks:
+                continue
+            b = np.array([ref.append(int(s)) for s in ids], np.int32)
+            assert np.array_equal(a, b)
+            for s in ids:
+                live[int(s)] += 1
+        elif op == 3:                                         # free one
+            s = int(rng.choice(list(live)))
+            prod.pa_alloc_free_seq(s)
+            ref.free_seq(s)
+            del live[s]
+        else:                                                 # reserve ahead (with COW)
+            ids = rng.choice(list(live), size=min(len(live), 3), replace=False).astype(np.int32)
+            extra = int(rng.integers(1, 20))
+            try:
+                prod.pa_alloc_reserve_batch(ids, extra)
+            except pa.PANoBlocks:
+                continue
+            for s in ids:
+                ref.reserve(int(s), extra)
+        assert prod.num_free == ref.num_free, step
+        if step % 50 == 0:
+            assert np.array_equal(prod.pa_alloc_take_copies(), ref.take_copies())
+    assert np.array_equal(prod.pa_alloc_take_copies(), ref.take_copies())
+    ids = np.array(sorted(live), np.int32)
+    if ids.size:
+        width = max(8, max((live[int(s)] + 40) // bs for s in ids))
+        assert np.array_equal(prod.pa_alloc_block_tables(ids, width), ref.block_tables(ids, width))
+        assert np.array_equal(prod.pa_alloc_context_lens(ids), ref.context_lens(ids))
+    for b in range(NB):
+        assert prod.pa_alloc_refcount(b) == ref.refcount(b)
+    used = sum(1 for b in range(NB) if prod.pa_alloc_refcount(b) > 0)
+    assert used + prod.num_free == NB

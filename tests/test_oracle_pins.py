@@ -363,3 +363,60 @@ def test_allocator_reserve_then_appends_pop_nothing():
     for _ in range(7):                                   # positions 18 .. 24 -> block 3 popped
         al.append(0)
     assert al.num_free == 16
+
+
+# --------------------------------------------------------------------------- shared prefixes
+def test_fork_shares_blocks_and_copy_on_write_keeps_the_parent_intact():
+    bs = 8
+    al = oracle.Alloc(32, bs, seed=9)
+    al.add_seq(0, 20)                                    # blocks b0 b1 b2 (b2 partial: 4 rows)
+    parent = al.block_tables([0], 3)[0].copy()
+    free0 = al.num_free
+    al.fork(0, 1, 20)                                    # child shares all three
+    assert al.num_free == free0
+    assert np.array_equal(al.block_tables([1], 3)[0], parent)
+    assert [al.refcount(int(b)) for b in parent] == [2, 2, 2]
+    slot = al.append(1)                                  # position 20 lands in shared b2 -> COW
+    child = al.block_tables([1], 3)[0]
+    assert np.array_equal(child[:2], parent[:2]) and child[2] != parent[2]
+    assert al.refcount(int(parent[2])) == 1 and al.refcount(int(child[2])) == 1
+    assert slot == child[2] * bs + 4
+    assert al.take_copies().tolist() == [[int(parent[2]), int(child[2])]]
+    assert al.take_copies().shape == (0, 2)
+    assert np.array_equal(al.block_tables([0], 3)[0], parent)        # parent untouched
+    al.append(0)                                         # parent's b2 is private again: no COW
+    assert al.take_copies().shape == (0, 2)
+    al.fork(0, 2, 16)                                    # block-aligned prefix: b0 b1 only
+    al.append(2)                                         # position 16 needs a fresh block
+    assert al.take_copies().shape == (0, 2)
+    for s in (0, 1, 2):
+        al.free_seq(s)
+    assert al.num_free == 32                             # every block back exactly once
+
+
+def test_decode_over_a_fork_equals_dense_attention_over_its_tokens():
+    D, bs, Hq, Hkv = 16, 8, 4, 2
+    rng = np.random.default_rng(12)
+    draw = lambda shape: oracle.round_to(rng.standard_normal(shape), "f16")
+    nb = 16
+    kc = np.full((nb, Hkv, bs, D), 0x7E00, np.uint16)
+    vc = kc.copy()
+    al = oracle.Alloc(nb, bs, seed=4)
+    prefix_k, prefix_v = draw((13, Hkv, D)), draw((13, Hkv, D))
+    al.add_seq(0, 13)
+    oracle.reshape_and_cache(prefix_k, prefix_v, kc, vc, al.slots(0, 0, 13), bs)
+    al.fork(0, 1, 11)                                    # child keeps 11 prefix tokens
+    own_k, own_v = draw((5, Hkv, D)), draw((5, Hkv, D))
+    slots = np.array([al.append(1) for _ in range(5)], np.int32)
+    pairs = al.take_copies()
+    assert pairs.shape == (1, 2)                         # block 1 (rows 8..12) was shared
+    oracle.copy_blocks(kc, vc, pairs)
+    oracle.reshape_and_cache(own_k, own_v, kc, vc, slots, bs)
+    q = draw((2, Hq, D))
+    bt = al.block_tables([0, 1], 3)
+    lens = np.array([13, 16], np.int32)
+    got = oracle.decode_v1(q, kc, vc, bt, lens, np.float32(0.25), "f16")
+    kv = [(prefix_k, prefix_v),
+          (np.concatenate([prefix_k[:11], own_k]), np.concatenate([prefix_v[:11], own_v]))]
+    ref = _dense_reference(q, kv, lens, Hq, Hkv, 0.25, "f16")
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
