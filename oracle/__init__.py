@@ -86,6 +86,17 @@ def _load():
         lib.or_paged_decode_v1.restype = i32
         lib.or_paged_decode_v2.argtypes = dec + [i32]
         lib.or_paged_decode_v2.restype = i32
+        lib.or_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.or_e4m3_to_f64.restype = f64
+        lib.or_f64_to_e4m3.argtypes = [f64]
+        lib.or_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.or_e4m3_widen_array.argtypes = [P, P, i64]
+        lib.or_e4m3_round_array.argtypes = [P, P, i64]
+        lib.or_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32]
+        lib.or_reshape_and_cache_fp8.restype = i32
+        lib.or_paged_decode_fp8.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32,
+                                            f32, f32, f32, i32, P]
+        lib.or_paged_decode_fp8.restype = i32
         lib.or_splitmix64_next.argtypes = [ctypes.POINTER(u64)]
         lib.or_splitmix64_next.restype = u64
         lib.or_alloc_create.argtypes = [i32, i32, u64, i32]
@@ -143,6 +154,64 @@ def round_to(x: np.ndarray, dtype) -> np.ndarray:
     v = _c(x, np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
     lib.or_round_array(_ptr(v), _ptr(out), v.size, dtype_code(dtype))
+    return out
+
+
+def e4m3_widen(bits: np.ndarray) -> np.ndarray:
+    """fp8 E4M3 bit patterns (uint8) -> exact float64 values."""
+    lib = _load()
+    b = _c(bits, np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    lib.or_e4m3_widen_array(_ptr(b), _ptr(out), b.size)
+    return out
+
+
+def e4m3_round(x: np.ndarray) -> np.ndarray:
+    """float64 -> E4M3 bit patterns, nearest-even, saturating at +-448."""
+    lib = _load()
+    v = _c(x, np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib.or_e4m3_round_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def reshape_and_cache_fp8(key_bits, value_bits, key_cache8, value_cache8, slot_mapping,
+                          block_size: int, dtype, k_scale: float, v_scale: float) -> int:
+    """Quantising scatter of 16-bit rows [T, Hkv, D] into uint8 E4M3 pools, in place."""
+    lib = _load()
+    k = _c(key_bits, np.uint16)
+    v = _c(value_bits, np.uint16)
+    sm = _c(slot_mapping, np.int32)
+    assert key_cache8.dtype == np.uint8 and key_cache8.flags.c_contiguous
+    assert value_cache8.dtype == np.uint8 and value_cache8.flags.c_contiguous
+    T, Hkv, D = k.shape
+    NB = key_cache8.shape[0]
+    return int(lib.or_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(key_cache8), _ptr(value_cache8),
+                                            _ptr(sm), T, Hkv, D, block_size, NB, dtype_code(dtype),
+                                            float(k_scale), float(v_scale)))
+
+
+def decode_fp8(q_bits, k_cache8, v_cache8, block_tables, context_lens, scale, k_scale, v_scale,
+               dtype, only=None) -> np.ndarray:
+    """Exact fp64 decode over fp8 E4M3 pools (dequantised by the per-tensor scales)."""
+    lib = _load()
+    q = _c(q_bits, np.uint16)
+    kc = _c(k_cache8, np.uint8)
+    vc = _c(v_cache8, np.uint8)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    S, Hq, D = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    only_arr = None if only is None else _c(only, np.uint8).reshape(S * Hq)
+    rc = lib.or_paged_decode_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                 _ptr(cl), S, Hq, Hkv, D, bs, NB, float(scale), float(k_scale),
+                                 float(v_scale), dtype_code(dtype),
+                                 _ptr(only_arr) if only_arr is not None else None)
+    if rc == -2:
+        raise ValueError("oracle: unsupported shapes")
+    if rc == -1:
+        raise IndexError("oracle: block table entry outside the pool")
     return out
 
 

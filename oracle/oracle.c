@@ -104,6 +104,48 @@ double or_bf16_to_f64(uint16_t b) { return bits_to_double(b, 7, 8); }
 uint16_t or_f64_to_f16(double x) { return double_to_bits(x, 10, 5); }
 uint16_t or_f64_to_bf16(double x) { return double_to_bits(x, 7, 8); }
 
+/* ------------------------------------------------------------------------- */
+/* fp8 E4M3 (OCP "E4M3FN"): 1 sign, 4 exponent (bias 7), 3 fraction bits; no     */
+/* infinities; S.1111.111 is NaN; largest finite 448.  Used for the fp8 KV cache   */
+/* the "vLLM Project Update" talk lists among the supported quantisation methods.  */
+/* ------------------------------------------------------------------------- */
+double or_e4m3_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1, e = (b >> 3) & 15, f = b & 7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) v = ldexp((double)f, -9);                 /* subnormal: f * 2^(1-7-3) */
+    else v = ldexp((double)(f | 8), e - 10);              /* (8+f) * 2^(e-7-3) */
+    return sign ? -v : v;
+}
+
+/* Round to E4M3, nearest with ties to even; finite values beyond 448 saturate to
+ * +-448 (the fp8 KV cache stores finite numbers only); NaN stays NaN. */
+uint8_t or_f64_to_e4m3(double x) {
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x)) return (uint8_t)(sign | 0x7F);
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);        /* 448 = 1.75 * 2^8 */
+    int e2;
+    (void)frexp(a, &e2);
+    int k = e2 - 1;                                       /* a in [2^k, 2^(k+1)) */
+    if (k < -6) k = -6;                                   /* subnormals share 2^-6's quantum */
+    double n = ldexp(a, 3 - k);
+    double r = nearbyint(n);
+    if (r >= 16.0) { r = 8.0; k += 1; }
+    if (k > 8 || (k == 8 && r > 14.0)) return (uint8_t)(sign | 0x7E);   /* rounds past 448 */
+    if (r < 8.0) return (uint8_t)(sign | (uint8_t)r);     /* subnormal (k == -6) */
+    return (uint8_t)(sign | (uint8_t)((k + 7) << 3) | (uint8_t)(r - 8.0));
+}
+
+void or_e4m3_widen_array(const uint8_t* in, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_e4m3_to_f64(in[i]);
+}
+
+void or_e4m3_round_array(const double* in, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_f64_to_e4m3(in[i]);
+}
+
 static double widen(uint16_t b, int dtype) {
     return dtype == OR_BF16 ? or_bf16_to_f64(b) : or_f16_to_f64(b);
 }
@@ -317,6 +359,94 @@ int32_t or_paged_decode_v2(double* out, const uint16_t* q, const uint16_t* k_cac
         free(op);
     }
     free(scratch);
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* fp8 KV cache.  Readings: per-tensor scales k_scale, v_scale (> 0); a cached      */
+/* element stores e4m3(x * inv) with inv = the fp32 reciprocal of the scale,       */
+/* correctly rounded, and x * inv rounded to fp32 first (one fp32 multiply, then   */
+/* rounding to E4M3, ties to even, saturating at 448); it reads back as            */
+/* decode(e4m3) * scale.  Queries and outputs stay 16-bit.                         */
+/* ------------------------------------------------------------------------- */
+static uint8_t quantize_e4m3(uint16_t x16, int dtype, float inv) {
+    float xf = (float)widen(x16, dtype);        /* exact */
+    float prod = xf * inv;                       /* fp32 product, correctly rounded */
+    return or_f64_to_e4m3((double)prod);
+}
+
+int32_t or_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, uint8_t* key_cache,
+                                 uint8_t* value_cache, const int32_t* slot_mapping,
+                                 int32_t num_tokens, int32_t num_kv_heads, int32_t head_size,
+                                 int32_t block_size, int32_t num_blocks, int32_t dtype,
+                                 float k_scale, float v_scale) {
+    float kinv = 1.0f / k_scale, vinv = 1.0f / v_scale;
+    int32_t bad = 0;
+    for (int32_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_blocks * block_size) { ++bad; continue; }
+        int64_t block = slot / block_size, offset = slot % block_size;
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            for (int32_t d = 0; d < head_size; ++d) {
+                int64_t src = ((int64_t)i * num_kv_heads + h) * head_size + d;
+                int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * head_size + d;
+                key_cache[dst] = quantize_e4m3(key[src], dtype, kinv);
+                value_cache[dst] = quantize_e4m3(value[src], dtype, vinv);
+            }
+    }
+    return bad;
+}
+
+/* Decode over an fp8 cache: the plain definition with k_t = decode(K8) * k_scale and
+ * v_t = decode(V8) * v_scale, everything else as or_paged_decode_v1. */
+int32_t or_paged_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_cache,
+                            const uint8_t* v_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_size, int32_t block_size, int32_t num_blocks, float scale,
+                            float k_scale, float v_scale, int32_t dtype, const uint8_t* only) {
+    if (check_shapes(num_q_heads, num_kv_heads, head_size, block_size)) return -2;
+    int32_t group = num_q_heads / num_kv_heads;
+    int bad = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t L = context_lens[s];
+        double* p = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            if (only && !only[(int64_t)s * num_q_heads + h]) continue;
+            double* o = out + ((int64_t)s * num_q_heads + h) * head_size;
+            for (int32_t d = 0; d < head_size; ++d) o[d] = 0.0;
+            if (L <= 0) continue;
+            int32_t kvh = h / group;
+            const uint16_t* qrow = q + ((int64_t)s * num_q_heads + h) * head_size;
+            double m = -INFINITY;
+            for (int32_t t = 0; t < L; ++t) {
+                int32_t phys = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                if (t / block_size >= max_blocks_per_seq || phys < 0 || phys >= num_blocks) {
+                    bad = 1;
+                    p[t] = -INFINITY;
+                    continue;
+                }
+                int64_t row = (((int64_t)phys * num_kv_heads + kvh) * block_size + t % block_size) * head_size;
+                double acc = 0.0;
+                for (int32_t d = 0; d < head_size; ++d)
+                    acc += widen(qrow[d], dtype) * (or_e4m3_to_f64(k_cache[row + d]) * (double)k_scale);
+                p[t] = (double)scale * acc;
+                if (p[t] > m) m = p[t];
+            }
+            double l = 0.0;
+            for (int32_t t = 0; t < L; ++t) { p[t] = exp(p[t] - m); l += p[t]; }
+            for (int32_t t = 0; t < L; ++t) {
+                int32_t phys = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                if (phys < 0 || phys >= num_blocks) continue;
+                int64_t row = (((int64_t)phys * num_kv_heads + kvh) * block_size + t % block_size) * head_size;
+                for (int32_t d = 0; d < head_size; ++d)
+                    o[d] += p[t] * (or_e4m3_to_f64(v_cache[row + d]) * (double)v_scale);
+            }
+            for (int32_t d = 0; d < head_size; ++d) o[d] /= l;
+        }
+        free(p);
+    }
     return bad ? -1 : 0;
 }
 

@@ -420,3 +420,69 @@ def test_decode_over_a_fork_equals_dense_attention_over_its_tokens():
           (np.concatenate([prefix_k[:11], own_k]), np.concatenate([prefix_v[:11], own_v]))]
     ref = _dense_reference(q, kv, lens, Hq, Hkv, 0.25, "f16")
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- fp8 E4M3
+def test_e4m3_widen_matches_torch_all_patterns():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    bits = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_widen(bits)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def test_e4m3_rounding_matches_torch_in_range_and_saturates_beyond():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(5)
+    x = np.ldexp(rng.random(100_000) + 1.0, rng.integers(-12, 9, size=100_000))
+    x *= rng.choice([-1.0, 1.0], size=x.size)
+    x = x[np.abs(x) < 464.0].astype(np.float32).astype(np.float64)   # below the overflow tie
+    ours = oracle.e4m3_round(x)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    # closed forms: ties to even, saturation, NaN
+    cases = [(1.0 + 1 / 16, 0x38), (1.0 + 3 / 16, 0x3A), (448.0, 0x7E), (460.0, 0x7E),
+             (1e6, 0x7E), (-1e6, 0xFE), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (3 * 2.0 ** -11, 0x01)]
+    for v, b in cases:
+        assert int(oracle.e4m3_round(np.array([v]))[0]) == b, v
+    assert int(oracle.e4m3_round(np.array([np.nan]))[0]) & 0x7F == 0x7F
+
+
+def test_fp8_cache_decode_equals_dense_attention_over_dequantised_values():
+    D, bs, Hq, Hkv = 32, 16, 8, 2
+    rng = np.random.default_rng(19)
+    lens = np.array([3, 16, 40], np.int32)
+    S = lens.size
+    nb = 8
+    ks, vs = np.float32(0.07), np.float32(0.05)
+    k16 = [oracle.round_to(rng.standard_normal((int(L), Hkv, D)), "bf16") for L in lens]
+    v16 = [oracle.round_to(rng.standard_normal((int(L), Hkv, D)), "bf16") for L in lens]
+    kc = np.zeros((nb, Hkv, bs, D), np.uint8)
+    vc = kc.copy()
+    al = oracle.Alloc(nb, bs, 2)
+    for s, L in enumerate(lens):
+        al.add_seq(s, int(L))
+        assert oracle.reshape_and_cache_fp8(k16[s], v16[s], kc, vc, al.slots(s, 0, int(L)), bs,
+                                            "bf16", ks, vs) == 0
+    bt = al.block_tables(np.arange(S), 3)
+    q = oracle.round_to(rng.standard_normal((S, Hq, D)), "bf16")
+    got = oracle.decode_fp8(q, kc, vc, bt, lens, np.float32(D ** -0.5), ks, vs, "bf16")
+    # dense reference on the dequantised contiguous rows: e4m3(x * (1/scale)) * scale
+    inv_k, inv_v = np.float32(1) / ks, np.float32(1) / vs
+    def deq(x16, inv, sc):
+        xf = oracle.widen(x16, "bf16").astype(np.float32)
+        return oracle.e4m3_widen(oracle.e4m3_round((xf * inv).astype(np.float64))) * float(sc)
+    g = Hq // Hkv
+    for s, L in enumerate(lens):
+        k = np.repeat(deq(k16[s], inv_k, ks), g, axis=1)
+        v = np.repeat(deq(v16[s], inv_v, vs), g, axis=1)
+        logits = np.einsum("hd,thd->ht", oracle.widen(q[s], "bf16"), k) * float(np.float32(D ** -0.5))
+        p = scipy.special.softmax(logits, axis=1)
+        np.testing.assert_allclose(got[s], np.einsum("ht,thd->hd", p, v), rtol=1e-12, atol=1e-13)
