@@ -424,7 +424,7 @@ def run_profile_case(args):
     from paged_kv_cache_187_gb300 import workloads as W
     from paged_kv_cache_187_gb300.runner import DecodeRunner
     w = W.WORKLOADS[args.profile_workload]
-    r = DecodeRunner(w, device="cuda").next_step()
+    r = DecodeRunner(w, device="cuda", kv_fp8=args.kv_fp8).next_step()
     r.run_reshape()
     del r.k_prefill, r.v_prefill          # not needed for decoding: keep the footprint small
     torch.cuda.empty_cache()
@@ -435,7 +435,8 @@ def run_profile_case(args):
         r.run_decode(variant, partition_size=args.partition_size)
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0
-    print(json.dumps({"profile_case": w.name, "variant": variant, "steps": args.steps,
+    print(json.dumps({"profile_case": w.name, "kv_fp8": bool(args.kv_fp8), "variant": variant,
+                      "steps": args.steps,
                       "warmup": args.warmup, "gqa_cuda_cores": bool(args.gqa_cuda_cores),
                       "bytes_per_decode": r.kv_bytes()}))
 
@@ -455,6 +456,8 @@ def main():
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--gqa-cuda-cores", action="store_true",
                     help="profile case: force the CUDA-core path for grouped-query heads")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="profile case: keep the KV pools in fp8 E4M3")
     args = ap.parse_args()
     if args.profile_workload:
         run_profile_case(args)

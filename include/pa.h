@@ -66,7 +66,10 @@ typedef enum {
     PA_ERR_WORKSPACE = 5      /* workspace NULL or smaller than *_workspace_size */
 } pa_status;
 
-typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+/* Element types.  PA_FP8_E4M3 (OCP E4M3FN: 1 sign, 4 exponent bits with bias 7, 3
+ * fraction bits, no infinities, largest finite 448) is a cache type only: see
+ * pa_reshape_and_cache_fp8 / pa_decode_fp8 / pa_copy_blocks. */
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /* Same type as cudaStream_t, so callers without CUDA headers can still link. */
 typedef struct CUstream_st* pa_stream;
@@ -164,6 +167,38 @@ pa_status pa_decode_auto(void* out, const void* query, const void* key_cache,
                          void* workspace, size_t workspace_bytes, int32_t* status_dev,
                          pa_stream stream);
 
+/* ------------------------------------------------------------------------------ */
+/* fp8 KV cache ([TALK]: fp8 KV cache among the supported quantisation methods)      */
+/* ------------------------------------------------------------------------------ */
+/* Pools of PA_FP8_E4M3 bytes, [num_blocks][num_kv_heads][block_size][head_size], with
+ * one dequantisation scale per pool (k_scale, v_scale > 0): a cached byte c stands for
+ * e4m3(c) * scale.
+ * pa_reshape_and_cache_fp8: like pa_reshape_and_cache, but key / value (fp16 or bf16,
+ * `dtype`) are quantised: each element x becomes e4m3(x * r), r = 1 / scale computed in
+ * fp32 (correctly rounded), x * r rounded to fp32, then to E4M3 nearest-even, saturating
+ * at +-448 (NaN stays NaN).  Bit-exact with that definition. */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int32_t* slot_mapping,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_size,
+                                   int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                                   float k_scale, float v_scale, int32_t* status_dev,
+                                   pa_stream stream);
+
+/* pa_decode_fp8: paged decode over fp8 pools: out = softmax(scale * q . (k_scale * k_t))
+ * (v_scale * v_t), query and out fp16 or bf16 (`dtype`), head_size 128.  variant 0 =
+ * pa_decode_auto's choice, 1 = V1, 2 = V2 with `partition_size`; workspace as for
+ * those (the same *_workspace_size calls apply).  Internally the K / V tiles are
+ * widened to fp16 (exact) and the query rounded to fp16, so queries beyond fp16's range
+ * (|q| > 65504) are not supported. */
+pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, const void* value_cache,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                        int32_t num_blocks, int32_t max_context_len, float scale, float k_scale,
+                        float v_scale, pa_dtype dtype, int32_t variant, int32_t partition_size,
+                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                        pa_stream stream);
+
 /* One decode step of the hot path on device buffers: pa_reshape_and_cache of the
  * step's new K/V rows, then pa_decode_auto, on the same stream. */
 pa_status pa_decode_step(void* out, const void* query, const void* key, const void* value,
@@ -257,7 +292,8 @@ pa_status pa_advance_step(int32_t* context_lens, int32_t* slot_mapping, const in
  * int32 array [num_pairs][2], e.g. the pairs pa_alloc_take_copies returned, copied to
  * the device; run it before reshape_and_cache writes into the new blocks.  Pairs
  * outside the pool are skipped and flagged PA_DEVERR_BAD_BLOCK; a block that is both a
- * source and a destination in one call races. */
+ * source and a destination in one call races.  dtype is the pools' element type
+ * (PA_F16, PA_BF16 or PA_FP8_E4M3). */
 pa_status pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* block_pairs,
                          int32_t num_pairs, int32_t num_kv_heads, int32_t head_size,
                          int32_t block_size, int32_t num_blocks, pa_dtype dtype,

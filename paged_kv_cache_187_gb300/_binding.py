@@ -26,6 +26,7 @@ PA_ERR_WORKSPACE = 5
 
 PA_F16 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 
 PA_DEVERR_BAD_SLOT = 1
 PA_DEVERR_BAD_BLOCK = 2
@@ -71,6 +72,10 @@ def _load():
         "pa_decode_auto_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
         "pa_decode_auto": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P,
                             sz, P, P], i32),
+        "pa_reshape_and_cache_fp8": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, P, P],
+                                     i32),
+        "pa_decode_fp8": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, f32, f32,
+                           i32, i32, i32, P, sz, P, P], i32),
         "pa_decode_step": ([P, P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
                             i32, P, sz, P, P], i32),
         "pa_decode_step_host_staging_size": ([i32, i32, i32, i32, i32], sz),
@@ -264,6 +269,56 @@ def pa_decode_auto(out, query, key_cache, value_cache, block_tables, context_len
                                dt, wp, wb, _opt_dev(status, "status"), _stream(stream)))
 
 
+def _u8(t, name):
+    """An fp8 E4M3 pool: a uint8 (or float8_e4m3fn) CUDA tensor."""
+    import torch
+    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise TypeError(f"{name} must be uint8 / float8_e4m3fn (fp8 E4M3 bytes), got {t.dtype}")
+    return _dev(t, name)
+
+
+def pa_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale: float,
+                             v_scale: float, status=None, stream=None):
+    """Quantising scatter: key/value [T, Hkv, D] fp16/bf16 -> fp8 E4M3 pools [NB, Hkv, bs, D]."""
+    import torch
+    T, Hkv, D = key.shape
+    NB, Hkv2, bs, D2 = key_cache.shape
+    if value.shape != key.shape or value_cache.shape != key_cache.shape or (Hkv2, D2) != (Hkv, D):
+        raise ValueError("reshape_and_cache_fp8: inconsistent shapes")
+    if slot_mapping.shape != (T,):
+        raise ValueError("reshape_and_cache_fp8: slot_mapping must be [num_tokens]")
+    _check(_lib.pa_reshape_and_cache_fp8(
+        _dev(key, "key"), _dev(value, "value"), _u8(key_cache, "key_cache"),
+        _u8(value_cache, "value_cache"), _dev(slot_mapping, "slot_mapping", torch.int32), T, Hkv, D,
+        bs, NB, _dt(key), float(k_scale), float(v_scale), _opt_dev(status, "status"),
+        _stream(stream)))
+
+
+_VARIANTS = {"auto": 0, "v1": 1, "v2": 2}
+
+
+def pa_decode_fp8(out, query, key_cache, value_cache, block_tables, context_lens,
+                  max_context_len: int, scale: float, k_scale: float, v_scale: float,
+                  variant: str = "auto", partition_size: int = 0, workspace=None, status=None,
+                  stream=None):
+    """Paged decode over fp8 E4M3 pools; query/out fp16 or bf16 [S, Hq, D]."""
+    import torch
+    S, Hq, D = query.shape
+    NB, Hkv, bs, D2 = key_cache.shape
+    if out.shape != query.shape or value_cache.shape != key_cache.shape or D2 != D:
+        raise ValueError("decode_fp8: inconsistent shapes")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("decode_fp8: block_tables [S, max_blocks] and context_lens [S] expected")
+    wp, wb = _ws(workspace)
+    _check(_lib.pa_decode_fp8(
+        _dev(out, "out"), _dev(query, "query"), _u8(key_cache, "key_cache"),
+        _u8(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev(context_lens, "context_lens", torch.int32), S, Hq, Hkv, D,
+        bs, NB, int(max_context_len), float(scale), float(k_scale), float(v_scale), _dt(query),
+        _VARIANTS[variant], int(partition_size or 0), wp, wb, _opt_dev(status, "status"),
+        _stream(stream)))
+
+
 def pa_decode_step(out, query, key, value, key_cache, value_cache, slot_mapping, block_tables,
                    context_lens, max_context_len: int, scale: float, workspace=None, status=None,
                    stream=None):
@@ -367,9 +422,10 @@ def pa_copy_blocks(key_cache, value_cache, block_pairs, status=None, stream=None
     NB, Hkv, bs, D = key_cache.shape
     if value_cache.shape != key_cache.shape or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
         raise ValueError("copy_blocks: pools [NB, Hkv, bs, D] and pairs [n, 2] expected")
+    dt = PA_FP8_E4M3 if key_cache.element_size() == 1 else _dt(key_cache)
     _check(_lib.pa_copy_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
                                _dev(block_pairs, "block_pairs", torch.int32),
-                               int(block_pairs.shape[0]), Hkv, D, bs, NB, _dt(key_cache),
+                               int(block_pairs.shape[0]), Hkv, D, bs, NB, dt,
                                _opt_dev(status, "status"), _stream(stream)))
 
 

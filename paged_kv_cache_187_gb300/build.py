@@ -24,6 +24,7 @@ SOURCES = [
     "pa_decode_f16_d128.cu",
     "pa_decode_bf16_d64.cu",
     "pa_decode_f16_d64.cu",
+    "pa_decode_fp8.cu",
     "pa_aux.cu",
     "pa_noalloc.cu",
     "pa_host.cpp",

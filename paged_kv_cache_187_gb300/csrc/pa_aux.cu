@@ -1,7 +1,7 @@
 // pa_aux.cu -- the small kernels around the decode kernel:
 //   * reshape_and_cache: scatters each step's new K/V rows into the paged pools through
 //     slot_mapping ("[core] Multi Step Scheduling #7000", the slot_mapping / block_tables
-//     metadata a decode step carries);
+//     metadata a decode step carries), as-is or quantised to fp8 E4M3;
 //   * plan: lists the V2 partitions of every sequence ("vLLM Project Update" talk, the V2
 //     kernel that partitions sequences and spreads them over SMs) in claim order and
 //     resets the counters the decode kernel uses.
@@ -56,6 +56,49 @@ __global__ void __launch_bounds__(128)
         const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * row_chunks + dc;
         if (is_v) value_cache[dst] = __ldg(value + src);
         else key_cache[dst] = __ldg(key + src);
+    }
+}
+
+// Quantising scatter for an fp8 E4M3 cache: each element stores
+// e4m3(x * inv_scale), the fp32 product rounded to E4M3 nearest-even and saturated at
+// +-448 (fp8 KV cache, "vLLM Project Update" talk).  One CTA per new token; a thread
+// takes 8 elements (16 bytes in, 8 bytes out).
+template <bool SRC_BF16>
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                 uint2* __restrict__ key_cache, uint2* __restrict__ value_cache,
+                                 const int32_t* __restrict__ slot_mapping, int32_t num_kv_heads,
+                                 int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                 float k_inv, float v_inv, int32_t* status) {
+    allow_dependent_launch();
+    const int32_t i = blockIdx.x;
+    const int64_t slot = slot_mapping[i];
+    if (slot < 0) return;
+    if (slot >= (int64_t)num_blocks * block_size) {
+        if (threadIdx.x == 0 && status) atomicOr(status, kBadSlot);
+        return;
+    }
+    const int64_t block = slot / block_size, offset = slot % block_size;
+    const int32_t row_chunks = head_size / 8;
+    const int32_t per_tensor = num_kv_heads * row_chunks;
+    for (int32_t c = threadIdx.x; c < 2 * per_tensor; c += blockDim.x) {
+        const bool is_v = c >= per_tensor;
+        const int32_t r = is_v ? c - per_tensor : c;
+        const int32_t h = r / row_chunks, dc = r % row_chunks;
+        const int64_t src = ((int64_t)i * num_kv_heads + h) * row_chunks + dc;
+        const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * row_chunks + dc;
+        const uint4 x = __ldg((is_v ? value : key) + src);
+        const float inv = is_v ? v_inv : k_inv;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a, b;
+            unpack2<SRC_BF16>(w[j], a, b);
+            q[j] = f32x2_to_e4m3x2(__fmul_rn(a, inv), __fmul_rn(b, inv));
+        }
+        const uint2 out = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        (is_v ? value_cache : key_cache)[dst] = out;
     }
 }
 
@@ -316,6 +359,21 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
         static_cast<const uint4*>(key), static_cast<const uint4*>(value),
         static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), slot_mapping,
         num_kv_heads, head_size, block_size, num_blocks, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                         void* value_cache, const int32_t* slot_mapping,
+                                         int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                         bool src_bf16, float k_inv_scale, float v_inv_scale,
+                                         int32_t* status, cudaStream_t stream) {
+    if (num_tokens <= 0) return cudaSuccess;
+    auto kern = src_bf16 ? reshape_and_cache_fp8_kernel<true> : reshape_and_cache_fp8_kernel<false>;
+    kern<<<num_tokens, 128, 0, stream>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+        static_cast<uint2*>(key_cache), static_cast<uint2*>(value_cache), slot_mapping,
+        num_kv_heads, head_size, block_size, num_blocks, k_inv_scale, v_inv_scale, status);
     return cudaGetLastError();
 }
 

@@ -41,6 +41,11 @@ namespace pa {
 #define PA_DEVERR_BAD_LEN_ 4
 #define PA_DEVERR_TIMEOUT_ 8
 
+// Resident CTAs per SM the register allocation of 4-consumer fp8 kernels is sized for.
+#ifndef PA_FP8_MIN_CTAS
+#define PA_FP8_MIN_CTAS 3
+#endif
+
 // Tiles of the current unit still to issue when the producer claims the next unit.
 #ifndef PA_CLAIM_LEAD
 #define PA_CLAIM_LEAD 8
@@ -109,22 +114,28 @@ struct UnitDesc {
     int32_t pad;
 };
 
-template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_, int NCONS_>
+template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_, int NCONS_,
+          bool KV8_ = false>
 struct DecodeCfg {
     static constexpr int D = D_;
     static constexpr int BS = BS_;
-    static constexpr bool kBf16 = BF16_;
+    static constexpr bool kBf16 = BF16_;           // query / output type (bf16 or fp16)
+    static constexpr bool kKv8 = KV8_;             // K/V cache in fp8 E4M3 (else = query type)
     static constexpr bool kMma = MMA_;
     static constexpr int HCAP = HCAP_;             // query heads per unit the kernel holds
     static constexpr int NT = MMA_ ? HCAP_ / 8 : 0;  // mma n-tiles of 8 heads
     static constexpr int NSTAGE = NSTAGE_;
     static constexpr int NQ = NQ_;
     static constexpr int NCONS = NCONS_;           // consumer warps per CTA
-    static constexpr int HALVES = D / 64;          // 128-byte swizzle spans 64 elements
-    static constexpr int TILE_BYTES = D * BS * 2;  // one (block, kv head) tile of K or V
+    static constexpr int ELEM = KV8_ ? 1 : 2;      // bytes per cached element
+    static constexpr int HALVES = D * ELEM / 128;  // 128-byte swizzle spans per row
+    static constexpr int TILE_BYTES = D * BS * ELEM;  // one (block, kv head) tile of K or V
     static constexpr int HALF_BYTES = BS * 128;
     static constexpr int QROWS = HCAP;
     static constexpr int THREADS = 32 * (1 + NCONS);
+    // fp8 configurations run 4 consumer warps; cap their registers so that three CTAs
+    // (the shared-memory limit) still fit on an SM.
+    static constexpr int MIN_CTAS = (KV8_ && NCONS >= 4) ? PA_FP8_MIN_CTAS : 1;
     // per-lane floats of one consumer's softmax state (m, l, acc)
     static constexpr int NSTATE = MMA_ ? (4 * NT + (D / 16) * NT * 4) : (2 * HCAP_ + HCAP_ * (D / 32));
     static_assert(D == 64 || D == 128, "head_size");
@@ -137,6 +148,7 @@ struct DecodeCfg {
     // k - NSTAGE) belongs to the same consumer, so a consumer never waits on a stage that
     // is two phases behind -- where the mbarrier parity test would pass too early.
     static_assert(NSTAGE % NCONS == 0, "stages must be a multiple of the consumer warps");
+    static_assert(!KV8_ || D == 128, "fp8 K/V: head_size 128");
 };
 
 template <class C>
@@ -241,7 +253,7 @@ __device__ __forceinline__ void merge_partitions(const DecodeParams& p, const Un
     for (int i = 0; i < NI; ++i) {
         const int idx = lane + 32 * i;
         if (idx < g * CPH) {
-            const float inv = den[i] > 0.f ? 1.f / den[i] : 0.f;
+            const float inv = den[i] > 0.f ? p.out_scale / den[i] : 0.f;
             float v[4] = {a[i][0] * inv, a[i][1] * inv, a[i][2] * inv, a[i][3] * inv};
             store_row16<C>(p, u.seq, u.kvh * g + idx / CPH, (idx % CPH) * 4, v);
         }
@@ -271,9 +283,28 @@ __device__ __forceinline__ void finish_partition(const DecodeParams& p, const Un
 template <class C>
 struct MmaConsumer {
     static constexpr int D = C::D, BS = C::BS, NT = C::NT, KS = D / 16, MT = BS / 16;
+    // The mma operand type: the cache type for 16-bit caches; fp16 for fp8 caches (an
+    // E4M3 value converts to fp16 exactly, and the query is converted once per unit).
+    static constexpr bool kMmaBf16 = C::kBf16 && !C::kKv8;
+    // P enters the PV product as P_hi + P_lo unless the weights are fp16 (fp8 caches) and
+    // the output is bf16, where one fp16 term (2^-12) is already far below the output's
+    // own resolution.
+    static constexpr bool kSplitP = !(C::kKv8 && C::kBf16);
     uint32_t qb[NT][KS][2];
     float m[NT][2], l[NT][2];
     float acc[KS][NT][4];   // O^T fragments: rows = head dims, cols = query heads
+
+    // fp8 tiles are read with the head dims permuted so that every thread loads 16
+    // contiguous bytes (see tile_fp8); the dot product does not care about the order
+    // as long as Q uses the same one.  Dim of mma k-step i, lane quad q, element j:
+    static __device__ __forceinline__ int k_dim_fp8(int i, int q, int j) {
+        return 32 * q + 16 * (i >> 2) + 4 * (i & 3) + j;
+    }
+    // Output head dim of accumulator (m-tile i, lane, register r).
+    static __device__ __forceinline__ int out_dim(int i, int lane, int r) {
+        if constexpr (C::kKv8) return 32 * (i >> 1) + 4 * (lane >> 2) + 2 * (i & 1) + (r >> 1);
+        else return i * 16 + (lane >> 2) + 8 * (r >> 1);
+    }
 
     __device__ __forceinline__ void load_q(const uint8_t* qbuf, int group, int lane) {
 #pragma unroll
@@ -284,8 +315,17 @@ struct MmaConsumer {
                 uint32_t b0 = 0, b1 = 0;
                 if (row < group) {
                     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qbuf + (size_t)row * D * 2);
-                    b0 = q32[(16 * i + 2 * (lane & 3)) >> 1];
-                    b1 = q32[(16 * i + 8 + 2 * (lane & 3)) >> 1];
+                    if constexpr (C::kKv8) {
+                        const int d0 = k_dim_fp8(i, lane & 3, 0);
+                        float x0, x1, x2, x3;
+                        unpack2<C::kBf16>(q32[d0 >> 1], x0, x1);
+                        unpack2<C::kBf16>(q32[(d0 >> 1) + 1], x2, x3);
+                        b0 = pack2<false>(x0, x1);
+                        b1 = pack2<false>(x2, x3);
+                    } else {
+                        b0 = q32[(16 * i + 2 * (lane & 3)) >> 1];
+                        b1 = q32[(16 * i + 8 + 2 * (lane & 3)) >> 1];
+                    }
                 }
                 qb[nt][i][0] = b0;
                 qb[nt][i][1] = b1;
@@ -310,41 +350,15 @@ struct MmaConsumer {
     // One tile of BS tokens, `valid` (1..BS) of which belong to the unit.
     __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid,
                                          float scale_log2, int lane, float (*)[BS]) {
-        const int r8 = lane & 7, mi = lane >> 3;
-        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-        // S^T[token][head] = K Q^T, the head-dim steps split over two accumulator chains
-        // (even and odd steps) so that consecutive mma.sync do not wait on each other
-        float sc[MT][NT][4], sc2[MT][NT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) sc[mt][nt][r] = sc2[mt][nt][r] = 0.f;
-#pragma unroll
-        for (int i = 0; i < KS; ++i) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                uint32_t a[4];
-                const int t = mt * 16 + r8 + 8 * (mi & 1);
-                ldmatrix_x4(a, kbase + swz<C>(t, 2 * i + (mi >> 1)));
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (i & 1) mma_16816<C::kBf16>(sc2[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
-                    else mma_16816<C::kBf16>(sc[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
-                }
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) sc[mt][nt][r] += sc2[mt][nt][r];
-        // online softmax, per query head (columns 2*(lane&3) and +1 of each n-tile).  The
-        // weights enter the PV product as two 16-bit terms, P = P_hi + P_lo, so that their
-        // rounding to the operand type costs ~2^-17 instead of 2^-9 (bf16) of relative error.
-        uint32_t pb[MT][NT][2], pl[MT][NT][2];
+        if constexpr (C::kKv8) tile_fp8(kt, vt, valid, scale_log2, lane);
+        else tile16(kt, vt, valid, scale_log2, lane);
+    }
+
+    // Online softmax over the tile's scores sc (S^T fragments, raw dot products) and the
+    // hi / lo split of the weights into B fragments of the PV product.
+    __device__ __forceinline__ void softmax_tile(float (&sc)[MT][NT][4], int valid,
+                                                 float scale_log2, int lane,
+                                                 uint32_t (&pb)[MT][NT][2], uint32_t (&pl)[MT][NT][2]) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             float mx[2] = {-INFINITY, -INFINITY};
@@ -377,15 +391,20 @@ struct MmaConsumer {
                     sc[mt][nt][r] = e;
                     ps[r & 1] += e;
                 }
-                const uint32_t h01 = pack2<C::kBf16>(sc[mt][nt][0], sc[mt][nt][1]);
-                const uint32_t h23 = pack2<C::kBf16>(sc[mt][nt][2], sc[mt][nt][3]);
+                const uint32_t h01 = pack2<kMmaBf16>(sc[mt][nt][0], sc[mt][nt][1]);
+                const uint32_t h23 = pack2<kMmaBf16>(sc[mt][nt][2], sc[mt][nt][3]);
                 float r0, r1, r2, r3;
-                unpack2<C::kBf16>(h01, r0, r1);
-                unpack2<C::kBf16>(h23, r2, r3);
+                unpack2<kMmaBf16>(h01, r0, r1);
+                unpack2<kMmaBf16>(h23, r2, r3);
                 pb[mt][nt][0] = movmatrix_trans(h01);
                 pb[mt][nt][1] = movmatrix_trans(h23);
-                pl[mt][nt][0] = movmatrix_trans(pack2<C::kBf16>(sc[mt][nt][0] - r0, sc[mt][nt][1] - r1));
-                pl[mt][nt][1] = movmatrix_trans(pack2<C::kBf16>(sc[mt][nt][2] - r2, sc[mt][nt][3] - r3));
+                if constexpr (kSplitP) {
+                    pl[mt][nt][0] = movmatrix_trans(pack2<kMmaBf16>(sc[mt][nt][0] - r0, sc[mt][nt][1] - r1));
+                    pl[mt][nt][1] = movmatrix_trans(pack2<kMmaBf16>(sc[mt][nt][2] - r2, sc[mt][nt][3] - r3));
+                } else {
+                    pl[mt][nt][0] = pl[mt][nt][1] = 0u;
+                    (void)r0; (void)r1; (void)r2; (void)r3;
+                }
             }
             l[nt][0] = l[nt][0] * alpha[0] + ps[0];
             l[nt][1] = l[nt][1] * alpha[1] + ps[1];
@@ -397,6 +416,130 @@ struct MmaConsumer {
                 acc[i][nt][3] *= alpha[1];
             }
         }
+    }
+
+    // fp8 E4M3 tile [BS][128 B] (swizzled).  K: lane (g = lane/4, q = lane%4) reads 16
+    // contiguous bytes (k-steps 4h..4h+3 in the permuted head-dim order) of rows g and
+    // g+8 per 16-token group -- conflict-free, since the 128B swizzle puts the even and
+    // odd chunks of neighbouring rows in different banks.  V^T: for m-tile pair pp the
+    // lane reads 4 bytes (dims 32pp + 4g .. +3) of each of its tokens 2q, 2q+1, 2q+8,
+    // 2q+9 and assembles the fragments with byte permutes; the output dims come out in
+    // the matching order (out_dim).
+    __device__ __forceinline__ void tile_fp8(const uint8_t* kt, const uint8_t* vt, int valid,
+                                             float scale_log2, int lane) {
+        const int g = lane >> 2, q = lane & 3;
+        float sc[MT][NT][4], sc2[MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sc[mt][nt][r] = sc2[mt][nt][r] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int t0 = mt * 16 + g, t1 = t0 + 8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(kt + swz<C>(t0, 2 * q + h));
+                const uint4 w1 = *reinterpret_cast<const uint4*>(kt + swz<C>(t1, 2 * q + h));
+                const uint32_t u0[4] = {w0.x, w0.y, w0.z, w0.w};
+                const uint32_t u1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int i = 4 * h + s4;
+                    uint32_t a[4];
+                    e4m3x4_to_f16x2x2(u0[s4], a[0], a[2]);   // row g:   k 2q,2q+1 | 2q+8,2q+9
+                    e4m3x4_to_f16x2x2(u1[s4], a[1], a[3]);   // row g+8
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (i & 1) mma_16816<false>(sc2[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                        else mma_16816<false>(sc[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sc[mt][nt][r] += sc2[mt][nt][r];
+        uint32_t pb[MT][NT][2], pl[MT][NT][2];
+        softmax_tile(sc, valid, scale_log2, lane, pb, pl);
+        const bool ragged = valid < BS;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int tq = mt * 16 + 2 * q;
+            uint32_t keep0 = 0xffffffffu, keep8 = 0xffffffffu;
+            if (ragged) {
+                keep0 = ((tq < valid) ? 0x0000ffffu : 0u) | ((tq + 1 < valid) ? 0xffff0000u : 0u);
+                keep8 = ((tq + 8 < valid) ? 0x0000ffffu : 0u) | ((tq + 9 < valid) ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int pp = 0; pp < D / 32; ++pp) {
+                const int byte = 32 * pp + 4 * g;
+                const uint32_t v0 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq, byte >> 4) + (byte & 15));
+                const uint32_t v1 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq + 1, byte >> 4) + (byte & 15));
+                const uint32_t v8 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq + 8, byte >> 4) + (byte & 15));
+                const uint32_t v9 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq + 9, byte >> 4) + (byte & 15));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t a[4];
+                    // byte 2e+f of each token's word is head dim 32pp + 4g + 2e + f
+                    a[0] = e4m3x2_to_f16x2(__byte_perm(v0, v1, (2 * e) | ((4 + 2 * e) << 4))) & keep0;
+                    a[1] = e4m3x2_to_f16x2(__byte_perm(v0, v1, (2 * e + 1) | ((5 + 2 * e) << 4))) & keep0;
+                    a[2] = e4m3x2_to_f16x2(__byte_perm(v8, v9, (2 * e) | ((4 + 2 * e) << 4))) & keep8;
+                    a[3] = e4m3x2_to_f16x2(__byte_perm(v8, v9, (2 * e + 1) | ((5 + 2 * e) << 4))) & keep8;
+                    const int i = 2 * pp + e;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_16816<false>(acc[i][nt], a, pb[mt][nt][0], pb[mt][nt][1]);
+                        if constexpr (kSplitP)
+                            mma_16816<false>(acc[i][nt], a, pl[mt][nt][0], pl[mt][nt][1]);
+                    }
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void tile16(const uint8_t* kt, const uint8_t* vt, int valid,
+                                           float scale_log2, int lane) {
+        const int r8 = lane & 7, mi = lane >> 3;
+        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+        // S^T[token][head] = K Q^T, the head-dim steps split over two accumulator chains
+        // (even and odd steps) so that consecutive mma.sync do not wait on each other
+        float sc[MT][NT][4], sc2[MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sc[mt][nt][r] = sc2[mt][nt][r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                uint32_t a[4];
+                const int t = mt * 16 + r8 + 8 * (mi & 1);
+                ldmatrix_x4(a, kbase + swz<C>(t, 2 * i + (mi >> 1)));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (i & 1) mma_16816<C::kBf16>(sc2[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                    else mma_16816<C::kBf16>(sc[mt][nt], a, qb[nt][i][0], qb[nt][i][1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sc[mt][nt][r] += sc2[mt][nt][r];
+        // online softmax; the weights enter the PV product as two 16-bit terms, P = P_hi +
+        // P_lo, so that their rounding to the operand type costs ~2^-17 instead of 2^-9
+        // (bf16) of relative error.
+        uint32_t pb[MT][NT][2], pl[MT][NT][2];
+        softmax_tile(sc, valid, scale_log2, lane, pb, pl);
         // O^T[dim][head] += V^T P^T
         const bool ragged = valid < BS;
 #pragma unroll
@@ -493,12 +636,12 @@ struct MmaConsumer {
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int d = i * 16 + (lane >> 2) + 8 * (r >> 1);
+                    const int d = out_dim(i, lane, r);
                     const int h = nt * 8 + 2 * (lane & 3) + (r & 1);
                     float v = acc[i][nt][r];
                     if (final_out) {
                         const float den = lt[nt][r & 1];
-                        v = den > 0.f ? v / den : 0.f;
+                        v = den > 0.f ? v * p.out_scale / den : 0.f;
                     }
                     ostage[h * D + d] = v;
                 }
@@ -578,9 +721,14 @@ struct CoreConsumer {
 
     // Loads this lane's DPL elements of row t of a swizzled tile as fp32.
     __device__ __forceinline__ void load_row(const uint8_t* tile, int t, int lane, float (&x)[DPL]) {
-        const int byte = lane * DPL * 2;          // offset inside the unswizzled row
+        const int byte = lane * DPL * C::ELEM;    // offset inside the unswizzled row
         const uint8_t* ptr = tile + swz<C>(t, byte >> 4) + (byte & 15);
-        if constexpr (DPL == 4) {
+        if constexpr (C::kKv8) {                  // 4 fp8 E4M3 -> fp16 (exact) -> fp32
+            static_assert(DPL == 4, "fp8 rows: head_size 128");
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(ptr);
+            unpack2<false>(e4m3x2_to_f16x2(w & 0xffffu), x[0], x[1]);
+            unpack2<false>(e4m3x2_to_f16x2(w >> 16), x[2], x[3]);
+        } else if constexpr (DPL == 4) {
             const uint2 w = *reinterpret_cast<const uint2*>(ptr);
             unpack2<C::kBf16>(w.x, x[0], x[1]);
             unpack2<C::kBf16>(w.y, x[2], x[3]);
@@ -717,7 +865,7 @@ struct CoreConsumer {
             if (h >= g) continue;
             const size_t row = (size_t)u.kvh * g + h;
             if (final_out) {
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                const float inv = lt > 0.f ? p.out_scale / lt : 0.f;
                 uint16_t* o = reinterpret_cast<uint16_t*>(p.out) +
                               ((size_t)u.seq * p.num_q_heads + row) * D + lane * DPL;
                 if constexpr (DPL == 4) {
@@ -747,7 +895,7 @@ struct CoreConsumer {
 // The kernel.
 // ---------------------------------------------------------------------------------
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
                         const int32_t persistent, const int32_t num_units_v1) {

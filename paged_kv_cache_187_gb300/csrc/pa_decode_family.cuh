@@ -29,17 +29,29 @@ constexpr int stages_for() {
 
 // Consumer warps per CTA: the CUDA-core path needs more warps to keep up with HBM than
 // the tensor-core path does.
-template <bool MMA, int BS>
+#ifndef PA_FP8_MMA_CONSUMERS
+#define PA_FP8_MMA_CONSUMERS 4
+#endif
+#ifndef PA_FP8_CORE_CONSUMERS
+#define PA_FP8_CORE_CONSUMERS 3
+#endif
+
+template <bool MMA, int BS, bool KV8>
 constexpr int consumers_for() {
+    // fp8 tiles carry twice the tokens per byte: their consumers do about four times the
+    // work per byte of a 16-bit tile, so they get more warps (measured: 4 on the
+    // tensor-core path, 3 on the CUDA-core path).
+    if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS : PA_FP8_CORE_CONSUMERS;
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
 
-template <int D, int BS, bool BF16, bool MMA, int HCAP>
+template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
-    constexpr int kCons = consumers_for<MMA, BS>();
-    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D, BS, kCons>(), 2, kCons>;
+    constexpr int kCons = consumers_for<MMA, BS, KV8>();
+    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D * (KV8 ? 1 : 2) / 2, BS, kCons>(), 2,
+                        kCons, KV8>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
     static bool configured = false;   // per instantiation; attribute setting is idempotent
@@ -71,14 +83,14 @@ cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
     return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p, (int32_t)(persistent ? 1 : 0), num_units);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool KV8 = false>
 cudaError_t launch_family(const KernelKey& k, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const DecodeParams& p, bool persistent, int32_t num_units,
                           cudaStream_t stream, int32_t* occ) {
 #define PA_CASE(BS_, MMA_, H_)                                                            \
     if (k.block_size == BS_ && k.mma == MMA_ && k.heads_cap == H_)                        \
-        return launch_one<D, BS_, BF16, MMA_, H_>(kmap, vmap, p, persistent, num_units,   \
-                                                  stream, occ);
+        return launch_one<D, BS_, BF16, MMA_, H_, KV8>(kmap, vmap, p, persistent, num_units, \
+                                                       stream, occ);
     PA_CASE(16, true, 8)
     PA_CASE(16, true, 16)
     PA_CASE(16, false, 1)

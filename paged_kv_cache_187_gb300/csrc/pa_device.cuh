@@ -187,6 +187,31 @@ __device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
     }
 }
 
+// Two fp8 E4M3 values (low byte first) -> f16x2 (low half first), exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(r)
+        : "r"(two));
+    return r;
+}
+
+// Four fp8 E4M3 values of one 32-bit word -> two f16x2 (bytes 0,1 and bytes 2,3), exact;
+// the word is split into its 16-bit halves without extra instructions.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
+}
+
+// Two fp32 values -> two fp8 E4M3 (lo in bits 0..7), nearest-even, saturating at +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 template <bool kBf16>
 __device__ __forceinline__ uint16_t to16(float x) {
     uint16_t r;

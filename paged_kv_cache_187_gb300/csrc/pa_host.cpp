@@ -76,6 +76,9 @@ pa_status current_device(int* dev, DeviceInfo* info) {
 cudaError_t dispatch_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
                             const pa::DecodeParams& p, bool persistent, int32_t units,
                             cudaStream_t st, int32_t* occ) {
+    if (k.kv8)
+        return k.bf16 ? pa::launch_decode_fp8kv_bf16q(k, km, vm, p, persistent, units, st, occ)
+                      : pa::launch_decode_fp8kv_f16q(k, km, vm, p, persistent, units, st, occ);
     if (k.head_size == 128)
         return k.bf16 ? pa::launch_decode_bf16_d128(k, km, vm, p, persistent, units, st, occ)
                       : pa::launch_decode_f16_d128(k, km, vm, p, persistent, units, st, occ);
@@ -97,7 +100,7 @@ cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CU
 }
 
 int32_t ctas_per_sm(int dev, const pa::KernelKey& k) {
-    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)(k.head_size == 128) << 20 |
+    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.kv8 << 21 | (uint64_t)(k.head_size == 128) << 20 |
                          (uint64_t)(k.block_size == 32) << 19 | (uint64_t)k.bf16 << 18 |
                          (uint64_t)k.mma << 17 | (uint64_t)k.heads_cap;
     {
@@ -140,14 +143,16 @@ EncodeTiledFn encode_fn() {
 // (128 bytes, the swizzle span) by block_size rows, i.e. one half of a (block, head)
 // tile when head_size is 128.
 pa_status encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int32_t head_size,
-                          int32_t block_size) {
+                          int32_t block_size, bool kv8) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int32_t elem = kv8 ? 1 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)head_size * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)head_size * elem};
+    cuuint32_t box[2] = {128u / (cuuint32_t)elem, (cuuint32_t)block_size};   // 128 bytes wide
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(pool), dims, strides,
+    CUresult r = fn(map, kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                    const_cast<void*>(pool), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -166,9 +171,11 @@ struct DecodeArgs {
     int32_t num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks;
     int32_t max_context_len;
     float scale;
-    pa_dtype dtype;
+    pa_dtype dtype;        // query / output type
     int32_t* status;
     cudaStream_t stream;
+    bool kv8 = false;      // cache in fp8 E4M3, dequantised by k_scale / v_scale
+    float k_scale = 1.f, v_scale = 1.f;
 };
 
 pa_status check_decode(const DecodeArgs& a) {
@@ -178,6 +185,10 @@ pa_status check_decode(const DecodeArgs& a) {
     if (a.dtype != PA_F16 && a.dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "decode: dtype");
     if (a.head_size != 64 && a.head_size != 128)
         return fail(PA_ERR_UNSUPPORTED, "decode: head_size %d (64 or 128)", a.head_size);
+    if (a.kv8 && a.head_size != 128)
+        return fail(PA_ERR_UNSUPPORTED, "decode: an fp8 cache needs head_size 128");
+    if (a.kv8 && !(a.k_scale > 0.f && a.v_scale > 0.f))
+        return fail(PA_ERR_INVALID_ARG, "decode: k_scale and v_scale must be positive");
     if (a.block_size != 16 && a.block_size != 32)
         return fail(PA_ERR_UNSUPPORTED, "decode: block_size %d (16 or 32)", a.block_size);
     if (a.num_q_heads % a.num_kv_heads)
@@ -202,6 +213,7 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
     k.head_size = a.head_size;
     k.block_size = a.block_size;
     k.bf16 = a.dtype == PA_BF16;
+    k.kv8 = a.kv8;
     const int g = a.num_q_heads / a.num_kv_heads;
     k.mma = g >= 2 && (g > 8 || g_gqa_mma);
     if (k.mma) k.heads_cap = g <= 8 ? 8 : 16;
@@ -224,16 +236,17 @@ pa::DecodeParams base_params(const DecodeArgs& a) {
     p.num_blocks = a.num_blocks;
     p.block_size = a.block_size;
     p.max_context_len = a.max_context_len;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.scale_log2 = a.scale * (a.kv8 ? a.k_scale : 1.f) * 1.4426950408889634f;
+    p.out_scale = a.kv8 ? a.v_scale : 1.f;
     p.status = a.status;
     return p;
 }
 
 pa_status make_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
     const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
-    pa_status st = encode_pool_map(km, a.key_cache, rows, a.head_size, a.block_size);
+    pa_status st = encode_pool_map(km, a.key_cache, rows, a.head_size, a.block_size, a.kv8);
     if (st != PA_OK) return st;
-    return encode_pool_map(vm, a.value_cache, rows, a.head_size, a.block_size);
+    return encode_pool_map(vm, a.value_cache, rows, a.head_size, a.block_size, a.kv8);
 }
 
 pa_status run_v1(const DecodeArgs& a) {
@@ -475,11 +488,12 @@ pa_status pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* bloc
                          int32_t* status_dev, pa_stream stream) {
     if (num_pairs < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
         return fail(PA_ERR_INVALID_ARG, "copy_blocks: sizes must be positive");
-    if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "copy_blocks: dtype");
+    if (dtype != PA_F16 && dtype != PA_BF16 && dtype != PA_FP8_E4M3)
+        return fail(PA_ERR_UNSUPPORTED, "copy_blocks: dtype");
     if (num_pairs == 0) return ok();
     if (!key_cache || !value_cache || !block_pairs)
         return fail(PA_ERR_INVALID_ARG, "copy_blocks: null pointer");
-    const int64_t bytes = (int64_t)num_kv_heads * block_size * head_size * 2;
+    const int64_t bytes = (int64_t)num_kv_heads * block_size * head_size * (dtype == PA_FP8_E4M3 ? 1 : 2);
     if (!aligned16(key_cache) || !aligned16(value_cache) || bytes % 16)
         return fail(PA_ERR_INVALID_ARG, "copy_blocks: pools must be 16-byte aligned, blocks 16-byte multiples");
     cudaError_t e = pa::launch_copy_blocks(key_cache, value_cache, block_pairs, num_pairs, bytes,
@@ -602,6 +616,59 @@ pa_status pa_decode_auto(void* out, const void* query, const void* key_cache,
     DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                  num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    if (v == 1) return run_v1(a);
+    return run_v2(a, P, workspace, workspace_bytes, /*adaptive=*/true);
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int32_t* slot_mapping,
+                                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_size,
+                                   int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                                   float k_scale, float v_scale, int32_t* status_dev,
+                                   pa_stream stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache_fp8: sizes must be positive");
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache_fp8: key/value must be fp16 or bf16");
+    if (head_size % 8) return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache_fp8: head_size % 8");
+    if (!(k_scale > 0.f && v_scale > 0.f))
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache_fp8: scales must be positive");
+    if (num_tokens == 0) return ok();
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache_fp8: null pointer");
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache_fp8: buffers must be 16-byte aligned");
+    const float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;   // correctly rounded fp32
+    cudaError_t e = pa::launch_reshape_and_cache_fp8(key, value, key_cache, value_cache,
+                                                     slot_mapping, num_tokens, num_kv_heads,
+                                                     head_size, block_size, num_blocks,
+                                                     dtype == PA_BF16, k_inv, v_inv, status_dev,
+                                                     (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache_fp8 launch");
+    return ok();
+}
+
+pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, const void* value_cache,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                        int32_t num_blocks, int32_t max_context_len, float scale, float k_scale,
+                        float v_scale, pa_dtype dtype, int32_t variant, int32_t partition_size,
+                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                        pa_stream stream) {
+    DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                 num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    a.kv8 = true;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    if (variant == 1) return run_v1(a);
+    if (variant == 2) return run_v2(a, partition_size, workspace, workspace_bytes);
+    if (variant != 0) return fail(PA_ERR_INVALID_ARG, "decode_fp8: variant must be 0, 1 or 2");
+    int32_t v = 0, P = 0;
+    pa_status st = pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                                       max_context_len, &v, &P);
+    if (st != PA_OK) return st;
     if (v == 1) return run_v1(a);
     return run_v2(a, P, workspace, workspace_bytes, /*adaptive=*/true);
 }

@@ -29,7 +29,9 @@ struct DecodeParams {
     int32_t num_blocks;
     int32_t block_size;
     int32_t max_context_len;
-    float scale_log2;             // softmax scale * log2(e): logits live in base-2 units
+    float scale_log2;             // softmax scale (x k_scale for fp8 caches) * log2(e):
+                                  // logits live in base-2 units
+    float out_scale;              // applied to every output row (v_scale for fp8 caches, else 1)
     int32_t partition_size;       // V2: tokens per partition (the smallest allowed when
                                   // adaptive); 0 = the whole context per unit (V1)
     int32_t adaptive;             // V2: 1 = the plan kernel sizes partitions from the lengths
@@ -55,7 +57,8 @@ WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32
 struct KernelKey {
     int32_t head_size;   // 64 | 128
     int32_t block_size;  // 16 | 32
-    bool bf16;
+    bool bf16;           // query / output type
+    bool kv8;            // cache in fp8 E4M3
     bool mma;            // tensor-core path (group >= 2) or CUDA-core path
     int32_t heads_cap;   // mma: 8 or 16 (n-tiles * 8); CUDA cores: 1, 2, 4 or 8
 };
@@ -98,5 +101,15 @@ cudaError_t launch_decode_f16_d64(const KernelKey&, const CUtensorMap&, const CU
                                   const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
 cudaError_t launch_decode_bf16_d64(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
                                    const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_fp8kv_f16q(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                     const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_fp8kv_bf16q(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                      const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                         void* value_cache, const int32_t* slot_mapping,
+                                         int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_size, int32_t block_size, int32_t num_blocks,
+                                         bool src_bf16, float k_inv_scale, float v_inv_scale,
+                                         int32_t* status, cudaStream_t stream);
 
 }  // namespace pa

@@ -24,10 +24,15 @@ from . import workloads as W
 class DecodeRunner:
     def __init__(self, w: W.Workload, device="cuda", rank: int = 0, poison: bool = True,
                  prefill_chunk_tokens: int = 65536, start_lens=None, num_blocks=None,
-                 alloc_seed=None):
+                 alloc_seed=None, kv_fp8: bool = False, k_scale: float = 0.02,
+                 v_scale: float = 0.02):
         """``start_lens`` / ``num_blocks`` / ``alloc_seed`` override the workload's own
-        (first-step context lengths including the new token, pool size, allocator seed)."""
+        (first-step context lengths including the new token, pool size, allocator seed).
+        ``kv_fp8`` keeps the pools in fp8 E4M3 with per-pool scales ``k_scale`` /
+        ``v_scale`` (queries, new rows and outputs stay in the workload's 16-bit type)."""
         self.w = w
+        self.kv_fp8 = kv_fp8
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
         self.device = torch.device(device)
         self.rank = rank
         S, bs = w.num_seqs, w.block_size
@@ -46,13 +51,18 @@ class DecodeRunner:
         for s in range(S):
             self.alloc.pa_alloc_add_seq(s, int(self.prefill_lens[s]))
         shape = (self.num_blocks, w.num_kv_heads, bs, w.head_size)
-        self.key_cache = torch.empty(shape, dtype=self.tdtype, device=self.device)
-        self.value_cache = torch.empty(shape, dtype=self.tdtype, device=self.device)
+        cdt = torch.uint8 if kv_fp8 else self.tdtype
+        self.key_cache = torch.empty(shape, dtype=cdt, device=self.device)
+        self.value_cache = torch.empty(shape, dtype=cdt, device=self.device)
         if poison:
-            nan = W.NAN_BITS[w.dtype]
-            nan = nan - 65536 if nan >= 32768 else nan
-            self.key_cache.view(torch.int16).fill_(nan)
-            self.value_cache.view(torch.int16).fill_(nan)
+            if kv_fp8:
+                self.key_cache.fill_(0x7F)          # E4M3 NaN
+                self.value_cache.fill_(0x7F)
+            else:
+                nan = W.NAN_BITS[w.dtype]
+                nan = nan - 65536 if nan >= 32768 else nan
+                self.key_cache.view(torch.int16).fill_(nan)
+                self.value_cache.view(torch.int16).fill_(nan)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         # prefill: tokens in sequence order, positions 0 .. L-2 of every sequence
         self.prefill_offsets = np.concatenate([[0], np.cumsum(self.prefill_lens)]).astype(np.int64)
@@ -67,8 +77,7 @@ class DecodeRunner:
         slots_d = torch.from_numpy(slots).to(self.device)
         for i in range(0, total, prefill_chunk_tokens):
             j = min(total, i + prefill_chunk_tokens)
-            B.pa_reshape_and_cache(self.k_prefill[i:j], self.v_prefill[i:j], self.key_cache,
-                                   self.value_cache, slots_d[i:j], status=self.status)
+            self._scatter(self.k_prefill[i:j], self.v_prefill[i:j], slots_d[i:j])
         self.step_index = -1
         self.out = torch.empty((S, w.num_q_heads, w.head_size), dtype=self.tdtype,
                                device=self.device)
@@ -102,15 +111,33 @@ class DecodeRunner:
     def step_max_context_len(self) -> int:
         return int(self.context_lens.max()) if self.context_lens.size else 0
 
+    def _scatter(self, k, v, slots_d, stream=None):
+        if self.kv_fp8:
+            B.pa_reshape_and_cache_fp8(k, v, self.key_cache, self.value_cache, slots_d,
+                                       self.k_scale, self.v_scale, status=self.status,
+                                       stream=stream)
+        else:
+            B.pa_reshape_and_cache(k, v, self.key_cache, self.value_cache, slots_d,
+                                   status=self.status, stream=stream)
+
     def run_reshape(self, stream=None):
-        B.pa_reshape_and_cache(self.k_new, self.v_new, self.key_cache, self.value_cache,
-                               self.slots_d, status=self.status, stream=stream)
+        self._scatter(self.k_new, self.v_new, self.slots_d, stream)
 
     def run_decode(self, variant: str = "auto", partition_size: int | None = None, stream=None,
                    max_context_len: int | None = None):
         mcl = self.step_max_context_len() if max_context_len is None else max_context_len
         args = (self.out, self.q, self.key_cache, self.value_cache, self.block_tables_d,
                 self.context_lens_d, mcl, self.w.scale)
+        if self.kv_fp8:
+            P = partition_size or (self.w.partition_size if variant == "v2" else 0)
+            if variant == "v2":
+                need = B.pa_decode_v2_workspace_size(self.w.num_seqs, self.w.num_q_heads,
+                                                     self.w.head_size, mcl, P)
+                if need > self.workspace.numel():
+                    self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+            B.pa_decode_fp8(*args, self.k_scale, self.v_scale, variant=variant, partition_size=P,
+                            workspace=self.workspace, status=self.status, stream=stream)
+            return
         if variant == "v1":
             B.pa_decode_v1(*args, status=self.status, stream=stream)
         elif variant == "v2":
@@ -126,7 +153,12 @@ class DecodeRunner:
             raise ValueError(variant)
 
     def run_step(self, stream=None):
-        """reshape_and_cache + pa_decode_auto through the single pa_decode_step call."""
+        """reshape_and_cache + pa_decode_auto through the single pa_decode_step call (for
+        fp8 pools: the fp8 scatter, then pa_decode_fp8's automatic choice)."""
+        if self.kv_fp8:
+            self.run_reshape(stream)
+            self.run_decode("auto", stream=stream)
+            return
         B.pa_decode_step(self.out, self.q, self.k_new, self.v_new, self.key_cache,
                          self.value_cache, self.slots_d, self.block_tables_d, self.context_lens_d,
                          self.step_max_context_len(), self.w.scale, workspace=self.workspace,
@@ -137,10 +169,10 @@ class DecodeRunner:
         """Algorithmic bytes of one decode step: every context token's K and V row of
         every kv head, plus the query and output rows."""
         w = self.w
-        elt = 2
+        elt = 1 if self.kv_fp8 else 2
         lens = self.context_lens.astype(np.int64)
         kv = int(lens.sum()) * w.num_kv_heads * w.head_size * 2 * elt
-        qo = 2 * w.num_seqs * w.num_q_heads * w.head_size * elt
+        qo = 2 * w.num_seqs * w.num_q_heads * w.head_size * 2
         return kv + qo
 
     def seq_tokens(self) -> int:
