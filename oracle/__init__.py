@@ -86,6 +86,9 @@ def _load():
         lib.or_paged_decode_v1.restype = i32
         lib.or_paged_decode_v2.argtypes = dec + [i32]
         lib.or_paged_decode_v2.restype = i32
+        lib.or_paged_decode_mq.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32,
+                                           i32, f32, i32]
+        lib.or_paged_decode_mq.restype = i32
         lib.or_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.or_e4m3_to_f64.restype = f64
         lib.or_f64_to_e4m3.argtypes = [f64]
@@ -154,6 +157,28 @@ def round_to(x: np.ndarray, dtype) -> np.ndarray:
     v = _c(x, np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
     lib.or_round_array(_ptr(v), _ptr(out), v.size, dtype_code(dtype))
+    return out
+
+
+def decode_mq(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens, scale, dtype):
+    """fp64 multi-query decode: q [S, q_len, Hq, D] -> [S, q_len, Hq, D]; new token j of a
+    sequence of length L attends to tokens t < L - q_len + j + 1."""
+    lib = _load()
+    q = _c(q_bits, np.uint16)
+    kc = _c(k_cache_bits, np.uint16)
+    vc = _c(v_cache_bits, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    S, QL, Hq, D = q.shape
+    NB, Hkv, bs, _ = kc.shape
+    out = np.zeros((S, QL, Hq, D), dtype=np.float64)
+    rc = lib.or_paged_decode_mq(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                _ptr(cl), S, QL, Hq, Hkv, D, bs, NB, float(scale),
+                                dtype_code(dtype))
+    if rc == -2:
+        raise ValueError("oracle: unsupported shapes")
+    if rc == -1:
+        raise IndexError("oracle: block table entry outside the pool")
     return out
 
 

@@ -362,6 +362,49 @@ int32_t or_paged_decode_v2(double* out, const uint16_t* q, const uint16_t* k_cac
     return bad ? -1 : 0;
 }
 
+/* Multi-query decode ([TALK]: kernels for several query tokens per sequence, used to
+ * verify speculative tokens).  Reading: every sequence brings the same number q_len of
+ * new tokens, already scattered, and context_lens[s] counts all of them; new token j
+ * (0-based) sits at position L - q_len + j and attends causally to tokens
+ * t < L - q_len + j + 1.  query / out are [num_seqs][q_len][num_q_heads][head_size].  A
+ * query row with no token to attend to (L < q_len - j) is a zero row. */
+int32_t or_paged_decode_mq(double* out, const uint16_t* q, const uint16_t* k_cache,
+                           const uint16_t* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                           int32_t num_blocks, float scale, int32_t dtype) {
+    int32_t rc = check_shapes(num_q_heads, num_kv_heads, head_size, block_size);
+    if (rc) return rc;
+    if (q_len <= 0) return -2;
+    decode_args a = {q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
+                     (double)scale, dtype};
+    int bad = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t L = context_lens[s];
+        double* scratch = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        for (int32_t j = 0; j < q_len; ++j) {
+            int32_t limit = L - q_len + j + 1;                  /* tokens this row sees */
+            for (int32_t h = 0; h < num_q_heads; ++h) {
+                double* o = out + (((int64_t)s * q_len + j) * num_q_heads + h) * head_size;
+                if (limit <= 0) {
+                    for (int32_t d = 0; d < head_size; ++d) o[d] = 0.0;
+                    continue;
+                }
+                /* the row's own query: a view of q with the multi-query layout */
+                decode_args aj = a;
+                aj.q = q + ((int64_t)s * q_len + j) * num_q_heads * head_size
+                         - (int64_t)s * num_q_heads * head_size;
+                double m, l;
+                attend_range(&aj, s, h, 0, limit, o, &m, &l, scratch, &bad);
+            }
+        }
+        free(scratch);
+    }
+    return bad ? -1 : 0;
+}
+
 /* ------------------------------------------------------------------------- */
 /* fp8 KV cache.  Readings: per-tensor scales k_scale, v_scale (> 0); a cached      */
 /* element stores e4m3(x * inv) with inv = the fp32 reciprocal of the scale,       */

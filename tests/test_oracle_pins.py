@@ -486,3 +486,27 @@ def test_fp8_cache_decode_equals_dense_attention_over_dequantised_values():
         logits = np.einsum("hd,thd->ht", oracle.widen(q[s], "bf16"), k) * float(np.float32(D ** -0.5))
         p = scipy.special.softmax(logits, axis=1)
         np.testing.assert_allclose(got[s], np.einsum("ht,thd->hd", p, v), rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- multi-query
+def test_multi_query_rows_equal_single_query_decodes_over_their_prefixes():
+    D, bs, Hq, Hkv, QL = 16, 8, 4, 2, 3
+    lens = np.array([3, 10, 17], np.int32)
+    q_single, kv, kc, vc, bt, lens = _paged_batch(lens, Hq, Hkv, D, bs, "bf16", seed=40,
+                                                  alloc_seed=41)
+    rng = np.random.default_rng(42)
+    q = oracle.round_to(rng.standard_normal((lens.size, QL, Hq, D)), "bf16")
+    got = oracle.decode_mq(q, kc, vc, bt, lens, np.float32(0.3), "bf16")
+    for j in range(QL):
+        # row j equals an ordinary decode whose context stops at L - QL + j + 1
+        ref = oracle.decode_v1(q[:, j], kc, vc, bt, lens - QL + j + 1, np.float32(0.3), "bf16")
+        assert np.array_equal(got[:, j], ref)
+    # and the dense reference with a causal mask, for the longest sequence
+    s = 2
+    k = np.repeat(oracle.widen(kv[s][0], "bf16"), Hq // Hkv, axis=1)
+    v = np.repeat(oracle.widen(kv[s][1], "bf16"), Hq // Hkv, axis=1)
+    for j in range(QL):
+        limit = int(lens[s]) - QL + j + 1
+        logits = np.einsum("hd,thd->ht", oracle.widen(q[s, j], "bf16"), k[:limit]) * float(np.float32(0.3))
+        ref = np.einsum("ht,thd->hd", scipy.special.softmax(logits, axis=1), v[:limit])
+        np.testing.assert_allclose(got[s, j], ref, rtol=1e-12, atol=1e-13)
