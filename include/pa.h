@@ -199,6 +199,35 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, con
                         void* workspace, size_t workspace_bytes, int32_t* status_dev,
                         pa_stream stream);
 
+/* ------------------------------------------------------------------------------ */
+/* Multi-query decode ([TALK], speculative decoding part: attention kernels for several */
+/* query tokens per sequence, to verify proposed tokens in one pass)                   */
+/* ------------------------------------------------------------------------------ */
+/* Every sequence brings q_len >= 1 new tokens, already in the pools (pa_reshape_and_cache
+ * with one slot per token), and context_lens[s] = L counts all of them.  New token j
+ * (0 <= j < q_len) sits at position L - q_len + j and attends to the tokens before and at
+ * it: out[s][j][h] = sum_t softmax_t(scale * q[s][j][h] . k_t) v_t over t < L - q_len + j
+ * + 1.  A row with no token to attend to (L < q_len - j) is a zero row.
+ *   query, out  [num_seqs][q_len][num_q_heads][head_size], fp16 or bf16 (`dtype`, also
+ *               the cache type); other arguments as for pa_decode_v1 / pa_decode_v2.
+ * The q_len * group rows of a (sequence, kv head) share one pass over its K/V on the
+ * tensor cores, 16 rows at a time (more rows re-read the K/V once per 16).  variant 0 =
+ * pa_decode_auto's choice (V1 or V2 with adaptive partitions), 1 = V1, 2 = V2 with
+ * `partition_size` tokens per partition.  q_len 1 is an ordinary decode.
+ * pa_decode_mq_workspace_size: the workspace for variant 2 with `partition_size`, or for
+ * variant 0 when partition_size is 0 (V1 needs none); 0 for bad sizes. */
+size_t pa_decode_mq_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                   int32_t max_context_len, int32_t partition_size);
+pa_status pa_decode_mq(void* out, const void* query, const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t q_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                       int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                       float scale, pa_dtype dtype, int32_t variant, int32_t partition_size,
+                       void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                       pa_stream stream);
+
 /* One decode step of the hot path on device buffers: pa_reshape_and_cache of the
  * step's new K/V rows, then pa_decode_auto, on the same stream. */
 pa_status pa_decode_step(void* out, const void* query, const void* key, const void* value,

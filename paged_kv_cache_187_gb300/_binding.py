@@ -76,6 +76,9 @@ def _load():
                                      i32),
         "pa_decode_fp8": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32, f32, f32,
                            i32, i32, i32, P, sz, P, P], i32),
+        "pa_decode_mq_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32], sz),
+        "pa_decode_mq": ([P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                          i32, i32, P, sz, P, P], i32),
         "pa_decode_step": ([P, P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f32,
                             i32, P, sz, P, P], i32),
         "pa_decode_step_host_staging_size": ([i32, i32, i32, i32, i32], sz),
@@ -317,6 +320,34 @@ def pa_decode_fp8(out, query, key_cache, value_cache, block_tables, context_lens
         bs, NB, int(max_context_len), float(scale), float(k_scale), float(v_scale), _dt(query),
         _VARIANTS[variant], int(partition_size or 0), wp, wb, _opt_dev(status, "status"),
         _stream(stream)))
+
+
+def pa_decode_mq_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads, head_size, block_size,
+                                max_context_len, partition_size=0) -> int:
+    return int(_lib.pa_decode_mq_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads,
+                                                head_size, block_size, max_context_len,
+                                                int(partition_size or 0)))
+
+
+def pa_decode_mq(out, query, key_cache, value_cache, block_tables, context_lens,
+                 max_context_len: int, scale: float, variant: str = "auto", partition_size: int = 0,
+                 workspace=None, status=None, stream=None):
+    """Multi-query paged decode: query/out [S, q_len, Hq, D]; new token j of a sequence of
+    length L attends to tokens t < L - q_len + j + 1."""
+    import torch
+    S, QL, Hq, D = query.shape
+    NB, Hkv, bs, D2 = key_cache.shape
+    if out.shape != query.shape or value_cache.shape != key_cache.shape or D2 != D:
+        raise ValueError("decode_mq: inconsistent shapes")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("decode_mq: block_tables [S, max_blocks] and context_lens [S] expected")
+    wp, wb = _ws(workspace)
+    _check(_lib.pa_decode_mq(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev(context_lens, "context_lens", torch.int32), S, QL, Hq,
+        Hkv, D, bs, NB, int(max_context_len), float(scale), _dt(query), _VARIANTS[variant],
+        int(partition_size or 0), wp, wb, _opt_dev(status, "status"), _stream(stream)))
 
 
 def pa_decode_step(out, query, key, value, key_cache, value_cache, slot_mapping, block_tables,

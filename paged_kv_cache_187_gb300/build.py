@@ -25,6 +25,8 @@ SOURCES = [
     "pa_decode_bf16_d64.cu",
     "pa_decode_f16_d64.cu",
     "pa_decode_fp8.cu",
+    "pa_decode_mq_f16.cu",
+    "pa_decode_mq_bf16.cu",
     "pa_aux.cu",
     "pa_noalloc.cu",
     "pa_host.cpp",

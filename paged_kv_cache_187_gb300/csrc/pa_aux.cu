@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         if ((tid & 31) == 0) atomicAdd(&total_tokens, mine);   // one shared atomic per warp
         __syncthreads();
         if (tid == 0) {
-            const unsigned long long work = total_tokens * (unsigned long long)p.num_kv_heads;
+            const unsigned long long work =
+                total_tokens * (unsigned long long)p.num_kv_heads * (unsigned long long)p.row_chunks;
             const unsigned long long want = (unsigned long long)max(p.grid_ctas, 1) * PA_UNITS_PER_CTA;
             unsigned long long Pa = (work / want / (unsigned)bs) * (unsigned)bs;
             if (Pa > (1ull << 30)) Pa = 1ull << 30;
@@ -236,11 +237,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         carry_np += tp;
         carry_nf += tf;
     }
-    const int32_t pairs = p.num_seqs * p.num_kv_heads;
+    const int32_t pairs = p.num_seqs * p.num_kv_heads * p.row_chunks;
     for (int32_t i = tid; i < pairs; i += blockDim.x) p.arrive[i] = 0;
     if (tid == 0) {
         p.hdr->total_parts = (uint32_t)parts;
-        p.hdr->total_units = (uint32_t)parts * (uint32_t)p.num_kv_heads;
+        p.hdr->total_units = (uint32_t)parts * (uint32_t)p.num_kv_heads * (uint32_t)p.row_chunks;
         p.hdr->partition_size = (uint32_t)P;
         p.hdr->counter = 0;
     }

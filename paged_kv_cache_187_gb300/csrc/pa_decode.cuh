@@ -6,7 +6,8 @@
 //     out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) v_t,   t < context_len[s],
 // where token t lives in row t % block_size of physical block block_tables[s][t / bs],
 // kv head h / group.  A work unit is (sequence, kv head, token range): the whole
-// context (V1) or one partition of partition_size tokens (V2).  A V2 unit of a sequence
+// context (V1) or one partition of partition_size tokens (V2); multi-query units also
+// carry a chunk of the (query token, head) rows.  A V2 unit of a sequence
 // with several partitions stores its partial (max, exp-sum, unnormalised sum); the last
 // unit of that (sequence, kv head) to finish merges all partials by log-sum-exp, so no
 // separate reduction launch is needed.
@@ -24,6 +25,9 @@
 //         P moved from accumulator to operand layout with movmatrix;
 //       - group 1 (MHA) or on request: CUDA cores, each lane owning head_size/32 dims,
 //         dot products finished by a transposed butterfly reduction;
+//       - several query tokens per sequence (multi-query, to verify speculative
+//         tokens): the tensor-core path with (query token, head) pairs on N, each
+//         column masked causally at its own token limit;
 //   * all barrier waits are bounded; a timeout is reported, never hung on.
 #pragma once
 
@@ -111,18 +115,22 @@ struct UnitDesc {
     int32_t pslot;   // partition slot for partial results, -1: write the final output
     int32_t pbase;   // first partition slot of the sequence
     int32_t nparts;  // partitions of the sequence
-    int32_t pad;
+    int32_t row0;    // first query row of the unit (rows: see DecodeParams)
+    int32_t nrows;   // query rows of the unit
+    int32_t len;     // context length of the sequence (multi-query causal limits)
+    int32_t pad[2];
 };
 
 template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_, int NCONS_,
-          bool KV8_ = false>
+          bool KV8_ = false, bool MQ_ = false>
 struct DecodeCfg {
     static constexpr int D = D_;
     static constexpr int BS = BS_;
     static constexpr bool kBf16 = BF16_;           // query / output type (bf16 or fp16)
     static constexpr bool kKv8 = KV8_;             // K/V cache in fp8 E4M3 (else = query type)
     static constexpr bool kMma = MMA_;
-    static constexpr int HCAP = HCAP_;             // query heads per unit the kernel holds
+    static constexpr bool kMq = MQ_;               // several causal query tokens per sequence
+    static constexpr int HCAP = HCAP_;             // query rows per unit the kernel holds
     static constexpr int NT = MMA_ ? HCAP_ / 8 : 0;  // mma n-tiles of 8 heads
     static constexpr int NSTAGE = NSTAGE_;
     static constexpr int NQ = NQ_;
@@ -149,6 +157,7 @@ struct DecodeCfg {
     // is two phases behind -- where the mbarrier parity test would pass too early.
     static_assert(NSTAGE % NCONS == 0, "stages must be a multiple of the consumer warps");
     static_assert(!KV8_ || D == 128, "fp8 K/V: head_size 128");
+    static_assert(!MQ_ || (MMA_ && !KV8_), "multi-query: tensor-core path, 16-bit cache");
 };
 
 template <class C>
@@ -181,10 +190,27 @@ __device__ __forceinline__ uint32_t swz(int t, int c16) {
 // ---------------------------------------------------------------------------------
 // Output / partial writers shared by both consumer types.
 // ---------------------------------------------------------------------------------
+// Row of `out` (in rows of head_size) that query row u.row0 + h of a unit goes to.
 template <class C>
-__device__ __forceinline__ void store_row16(const DecodeParams& p, int32_t seq, int32_t head,
-                                            int d0, const float (&v)[4]) {
-    uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + ((size_t)seq * p.num_q_heads + head) * C::D + d0;
+__device__ __forceinline__ size_t out_row(const DecodeParams& p, const UnitDesc& u, int h) {
+    if constexpr (C::kMq) {
+        const int r = u.row0 + h, j = r / p.group;
+        return ((size_t)u.seq * p.q_len + j) * p.num_q_heads + (size_t)u.kvh * p.group + (r - j * p.group);
+    } else {
+        return (size_t)u.seq * p.num_q_heads + (size_t)u.kvh * p.group + h;
+    }
+}
+
+// Row of the partial buffers (part_acc / part_ml) of query row u.row0 + h in slot pslot.
+__device__ __forceinline__ size_t part_row(const DecodeParams& p, const UnitDesc& u, int32_t pslot,
+                                          int h) {
+    return ((size_t)pslot * p.num_kv_heads + u.kvh) * p.rows + u.row0 + h;
+}
+
+template <class C>
+__device__ __forceinline__ void store_row16(const DecodeParams& p, size_t row, int d0,
+                                            const float (&v)[4]) {
+    uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + row * C::D + d0;
     uint2 w;
     w.x = pack2<C::kBf16>(v[0], v[1]);
     w.y = pack2<C::kBf16>(v[2], v[3]);
@@ -200,7 +226,7 @@ template <class C>
 __device__ __forceinline__ void merge_partitions(const DecodeParams& p, const UnitDesc& u, int lane) {
     constexpr int CPH = C::D / 4;                         // 4-dim chunks per head
     constexpr int NI = (C::HCAP * CPH + 31) / 32;         // chunks per lane, at most
-    const int g = p.group;
+    const int nr = u.nrows;
     const int np = u.nparts;
     float M[NI], den[NI], a[NI][4];
 #pragma unroll
@@ -220,8 +246,8 @@ __device__ __forceinline__ void merge_partitions(const DecodeParams& p, const Un
                 const int j = j0 + jj;
                 ml[jj][i] = make_float2(-INFINITY, 0.f);
                 x[jj][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < np && idx < g * CPH) {
-                    const size_t row = (size_t)(u.pbase + j) * p.num_q_heads + u.kvh * g + idx / CPH;
+                if (j < np && idx < nr * CPH) {
+                    const size_t row = part_row(p, u, u.pbase + j, idx / CPH);
                     ml[jj][i] = __ldcg(&p.part_ml[row]);
                     x[jj][i] = __ldcg(reinterpret_cast<const float4*>(p.part_acc + row * C::D) + idx % CPH);
                 }
@@ -252,10 +278,10 @@ __device__ __forceinline__ void merge_partitions(const DecodeParams& p, const Un
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
         const int idx = lane + 32 * i;
-        if (idx < g * CPH) {
+        if (idx < nr * CPH) {
             const float inv = den[i] > 0.f ? p.out_scale / den[i] : 0.f;
             float v[4] = {a[i][0] * inv, a[i][1] * inv, a[i][2] * inv, a[i][3] * inv};
-            store_row16<C>(p, u.seq, u.kvh * g + idx / CPH, (idx % CPH) * 4, v);
+            store_row16<C>(p, out_row<C>(p, u, idx / CPH), (idx % CPH) * 4, v);
         }
     }
 }
@@ -267,7 +293,8 @@ __device__ __forceinline__ void finish_partition(const DecodeParams& p, const Un
     __syncwarp();
     int last = 0;
     if (lane == 0) {
-        const int t = atomicAdd(&p.arrive[(size_t)u.seq * p.num_kv_heads + u.kvh], 1);
+        const size_t pair = ((size_t)u.seq * p.num_kv_heads + u.kvh) * p.row_chunks + u.row0 / C::HCAP;
+        const int t = atomicAdd(&p.arrive[pair], 1);
         last = (t == u.nparts - 1);
     }
     last = __shfl_sync(0xffffffffu, last, 0);
@@ -293,6 +320,8 @@ struct MmaConsumer {
     uint32_t qb[NT][KS][2];
     float m[NT][2], l[NT][2];
     float acc[KS][NT][4];   // O^T fragments: rows = head dims, cols = query heads
+    int32_t lim[NT][2];     // multi-query: tokens below lim[nt][j] are visible to this
+                            // lane's column nt*8 + 2*(lane%4) + j (causal, and < tok1)
 
     // fp8 tiles are read with the head dims permuted so that every thread loads 16
     // contiguous bytes (see tile_fp8); the dot product does not care about the order
@@ -306,14 +335,14 @@ struct MmaConsumer {
         else return i * 16 + (lane >> 2) + 8 * (r >> 1);
     }
 
-    __device__ __forceinline__ void load_q(const uint8_t* qbuf, int group, int lane) {
+    __device__ __forceinline__ void load_q(const uint8_t* qbuf, int nrows, int lane) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int row = nt * 8 + (lane >> 2);
 #pragma unroll
             for (int i = 0; i < KS; ++i) {
                 uint32_t b0 = 0, b1 = 0;
-                if (row < group) {
+                if (row < nrows) {
                     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qbuf + (size_t)row * D * 2);
                     if constexpr (C::kKv8) {
                         const int d0 = k_dim_fp8(i, lane & 3, 0);
@@ -333,6 +362,18 @@ struct MmaConsumer {
         }
     }
 
+    // Multi-query: query token j of a sequence of length L sits at position L - q_len + j
+    // and sees the tokens before and at it.
+    __device__ __forceinline__ void set_limits(const DecodeParams& p, const UnitDesc& u, int lane) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int r = u.row0 + nt * 8 + 2 * (lane & 3) + j;
+                lim[nt][j] = min(u.tok1, u.len - p.q_len + r / p.group + 1);
+            }
+    }
+
     __device__ __forceinline__ void reset() {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -347,16 +388,17 @@ struct MmaConsumer {
                 for (int r = 0; r < 4; ++r) acc[i][nt][r] = 0.f;
     }
 
-    // One tile of BS tokens, `valid` (1..BS) of which belong to the unit.
-    __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid,
+    // One tile of BS tokens starting at token tile0, `valid` (1..BS) of which belong to
+    // the unit.
+    __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid, int tile0,
                                          float scale_log2, int lane, float (*)[BS]) {
         if constexpr (C::kKv8) tile_fp8(kt, vt, valid, scale_log2, lane);
-        else tile16(kt, vt, valid, scale_log2, lane);
+        else tile16(kt, vt, valid, tile0, scale_log2, lane);
     }
 
     // Online softmax over the tile's scores sc (S^T fragments, raw dot products) and the
     // hi / lo split of the weights into B fragments of the PV product.
-    __device__ __forceinline__ void softmax_tile(float (&sc)[MT][NT][4], int valid,
+    __device__ __forceinline__ void softmax_tile(float (&sc)[MT][NT][4], int valid, int tile0,
                                                  float scale_log2, int lane,
                                                  uint32_t (&pb)[MT][NT][2], uint32_t (&pl)[MT][NT][2]) {
 #pragma unroll
@@ -368,18 +410,24 @@ struct MmaConsumer {
                 for (int r = 0; r < 4; ++r) {
                     const int tk = mt * 16 + (lane >> 2) + 8 * (r >> 1);
                     float v = sc[mt][nt][r] * scale_log2;
-                    v = tk < valid ? v : -INFINITY;
+                    bool keep;
+                    if constexpr (C::kMq) keep = tile0 + tk < lim[nt][r & 1];
+                    else keep = tk < valid;
+                    v = keep ? v : -INFINITY;
                     sc[mt][nt][r] = v;
                     mx[r & 1] = fmaxf(mx[r & 1], v);
                 }
-            float alpha[2];
+            float alpha[2], mref[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
                 mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
                 mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
                 const float mn = fmaxf(m[nt][j], mx[j]);
-                alpha[j] = fast_exp2(m[nt][j] - mn);
+                // A multi-query column may have seen no token yet (all masked so far):
+                // exponentiate against 0 then, so that its weights and rescale are 0, not NaN.
+                mref[j] = (C::kMq && mn == -INFINITY) ? 0.f : mn;
+                alpha[j] = fast_exp2(m[nt][j] - mref[j]);
                 m[nt][j] = mn;
             }
             float ps[2] = {0.f, 0.f};
@@ -387,7 +435,7 @@ struct MmaConsumer {
             for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const float e = fast_exp2(sc[mt][nt][r] - m[nt][r & 1]);
+                    const float e = fast_exp2(sc[mt][nt][r] - mref[r & 1]);
                     sc[mt][nt][r] = e;
                     ps[r & 1] += e;
                 }
@@ -465,7 +513,7 @@ struct MmaConsumer {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) sc[mt][nt][r] += sc2[mt][nt][r];
         uint32_t pb[MT][NT][2], pl[MT][NT][2];
-        softmax_tile(sc, valid, scale_log2, lane, pb, pl);
+        softmax_tile(sc, valid, 0, scale_log2, lane, pb, pl);
         const bool ragged = valid < BS;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -503,7 +551,7 @@ struct MmaConsumer {
     }
 
     __device__ __forceinline__ void tile16(const uint8_t* kt, const uint8_t* vt, int valid,
-                                           float scale_log2, int lane) {
+                                           int tile0, float scale_log2, int lane) {
         const int r8 = lane & 7, mi = lane >> 3;
         const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
         // S^T[token][head] = K Q^T, the head-dim steps split over two accumulator chains
@@ -539,7 +587,7 @@ struct MmaConsumer {
         // P_lo, so that their rounding to the operand type costs ~2^-17 instead of 2^-9
         // (bf16) of relative error.
         uint32_t pb[MT][NT][2], pl[MT][NT][2];
-        softmax_tile(sc, valid, scale_log2, lane, pb, pl);
+        softmax_tile(sc, valid, tile0, scale_log2, lane, pb, pl);
         // O^T[dim][head] += V^T P^T
         const bool ragged = valid < BS;
 #pragma unroll
@@ -646,34 +694,33 @@ struct MmaConsumer {
                     ostage[h * D + d] = v;
                 }
         __syncwarp();
-        const int g = p.group;
+        const int nr = u.nrows;
         if (final_out) {
-            uint16_t* out = reinterpret_cast<uint16_t*>(p.out) +
-                            ((size_t)u.seq * p.num_q_heads + (size_t)u.kvh * g) * D;
-            for (int c = lane; c < g * D / 8; c += 32) {
+            // rows of a unit are contiguous in `out` unless they span several query tokens
+            uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
+            for (int c = lane; c < nr * D / 8; c += 32) {
                 const float* src = ostage + c * 8;
                 uint4 w;
                 w.x = pack2<C::kBf16>(src[0], src[1]);
                 w.y = pack2<C::kBf16>(src[2], src[3]);
                 w.z = pack2<C::kBf16>(src[4], src[5]);
                 w.w = pack2<C::kBf16>(src[6], src[7]);
-                *reinterpret_cast<uint4*>(out + (size_t)c * 8) = w;
+                const int h = c / (D / 8);
+                *reinterpret_cast<uint4*>(out + out_row<C>(p, u, h) * D + (size_t)(c - h * (D / 8)) * 8) = w;
             }
         } else {
-            float* dst = p.part_acc + ((size_t)u.pslot * p.num_q_heads + (size_t)u.kvh * g) * D;
-            for (int c = lane; c < g * D / 4; c += 32)
+            float* dst = p.part_acc + part_row(p, u, u.pslot, 0) * D;
+            for (int c = lane; c < nr * D / 4; c += 32)
                 *reinterpret_cast<float4*>(dst + (size_t)c * 4) =
                     *reinterpret_cast<const float4*>(ostage + c * 4);
-            // (m, l) per head: lanes 0..3 hold heads 2*lane, 2*lane+1 of each n-tile
+            // (m, l) per row: lanes 0..3 hold columns 2*lane, 2*lane+1 of each n-tile
             if (lane < 4) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int h = nt * 8 + 2 * lane + j;
-                        if (h < g)
-                            p.part_ml[(size_t)u.pslot * p.num_q_heads + u.kvh * g + h] =
-                                make_float2(m[nt][j], lt[nt][j]);
+                        if (h < nr) p.part_ml[part_row(p, u, u.pslot, h)] = make_float2(m[nt][j], lt[nt][j]);
                     }
             }
             finish_partition<C>(p, u, lane);
@@ -692,14 +739,14 @@ struct CoreConsumer {
     float m[G], l[G];
     float acc[G][DPL];
 
-    __device__ __forceinline__ void load_q(const uint8_t* qbuf, int group, int lane) {
+    __device__ __forceinline__ void load_q(const uint8_t* qbuf, int nrows, int lane) {
         const uint16_t* q16 = reinterpret_cast<const uint16_t*>(qbuf);
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
             for (int j = 0; j < DPL; j += 2) {
                 float a = 0.f, b = 0.f;
-                if (h < group) {
+                if (h < nrows) {
                     const uint32_t w =
                         *reinterpret_cast<const uint32_t*>(q16 + (size_t)h * D + lane * DPL + j);
                     unpack2<C::kBf16>(w, a, b);
@@ -738,7 +785,7 @@ struct CoreConsumer {
         }
     }
 
-    __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid,
+    __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid, int,
                                          float scale_log2, int lane, float (*pbuf)[BS]) {
         // 1. logits: chunk tc of 8 tokens leaves token tc*8 + (lane >> 2) in this lane
         float lg[G][NC8];
@@ -935,6 +982,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
         const int32_t P = persistent ? (int32_t)p.hdr->partition_size : 0;
         const int32_t Hkv = p.num_kv_heads, g = p.group;
         const uint32_t qbytes = (uint32_t)(g * C::D * 2);
+        // work units per V2 list entry (per (sequence, kv head) in V1): the kv heads, and
+        // for multi-query kernels the chunks of query rows, chunk index fastest so that
+        // the chunks sharing a K/V stream are claimed together
+        const int32_t RC = C::kMq ? p.row_chunks : 1;
+        const int32_t upl = Hkv * RC;
         // Unit w as a descriptor: V1 units are (sequence, kv head) from the grid index;
         // V2 units come from the plan's list entry e (seq, partition, base slot, length).
         auto describe = [&](int32_t w, int4 e, bool done) {
@@ -946,12 +998,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             u.pslot = -1;
             u.pbase = 0;
             u.nparts = 1;
-            u.pad = 0;
+            u.row0 = 0;
+            u.nrows = g;
+            u.len = 0;
+            u.pad[0] = u.pad[1] = 0;
             if (!done) {
-                u.kvh = w % Hkv;
+                int32_t wu = w;
+                if constexpr (C::kMq) {
+                    wu = w / RC;
+                    u.row0 = (w - wu * RC) * C::HCAP;
+                    u.nrows = min(C::HCAP, p.rows - u.row0);
+                }
+                u.kvh = wu % Hkv;
                 if (!persistent) {
-                    u.seq = w / Hkv;
-                    u.tok1 = clamped_len(p, u.seq, u.kvh == 0);
+                    u.seq = wu / Hkv;
+                    u.tok1 = clamped_len(p, u.seq, u.kvh == 0 && u.row0 == 0);
+                    u.len = u.tok1;
                 } else {
                     u.seq = e.x;
                     u.tok0 = e.y * P;
@@ -959,6 +1021,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                     u.nparts = e.w > 0 ? (e.w + P - 1) / P : 1;
                     u.pbase = e.z;
                     u.pslot = u.nparts > 1 ? e.z + e.y : -1;
+                    u.len = e.w;
                 }
             }
             return u;
@@ -983,7 +1046,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
         int32_t claimed = 0;   // lane 0: raw result of the last atomic claim
         if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
         int32_t w = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : (int32_t)blockIdx.x;
-        int4 e = (persistent && w < total) ? p.part_list[w / Hkv] : kNoEntry;
+        int4 e = (persistent && w < total) ? p.part_list[w / upl] : kNoEntry;
         int32_t pre_phys = 0;       // prefetched first block-table chunk of unit w
         bool have_pre = false;
         uint32_t stage = 0, ephase = 1;
@@ -998,6 +1061,16 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                     sm.unit[qs] = u;
                     if (u.seq < 0) {
                         mbar_arrive(&sm.qfull[qs]);
+                    } else if constexpr (C::kMq) {
+                        // the unit's rows may span query tokens: one row copy each
+                        constexpr uint32_t kRowBytes = C::D * 2;
+                        mbar_arrive_expect_tx(&sm.qfull[qs], (uint32_t)u.nrows * kRowBytes);
+                        for (int h = 0; h < u.nrows; ++h) {
+                            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) +
+                                                 out_row<C>(p, u, h) * kRowBytes;
+                            bulk_load(sm.qbuf[qs] + h * kRowBytes, src, kRowBytes, &sm.qfull[qs]);
+                        }
+                        sm.qissued[qs] += 1;
                     } else {
                         mbar_arrive_expect_tx(&sm.qfull[qs], qbytes);
                         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) +
@@ -1032,7 +1105,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                     step = 1;
                 } else if (step == 1) {
                     w_next = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : total;
-                    e_next = (persistent && w_next < total) ? p.part_list[w_next / Hkv] : kNoEntry;
+                    e_next = (persistent && w_next < total) ? p.part_list[w_next / upl] : kNoEntry;
                     step = 2;
                 } else if (step == 2) {
                     if (w_next < total) {
@@ -1109,7 +1182,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             if (all_agree(!ok || sm.abort != 0)) break;
             const UnitDesc u = sm.unit[qs];
             if (u.seq < 0) break;
-            cons.load_q(sm.qbuf[qs], p.group, lane);
+            cons.load_q(sm.qbuf[qs], u.nrows, lane);
+            if constexpr (C::kMq) cons.set_limits(p, u, lane);
             __syncwarp();
             if (lane == 0) {
                 if (c == 0) sm.qconsumed[qs] += 1;
@@ -1129,8 +1203,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                     }
                     break;
                 }
-                const int valid = min(C::BS, u.tok1 - (b0 + j) * C::BS);
-                cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, p.scale_log2, lane, sm.pbuf[c]);
+                const int tile0 = (b0 + j) * C::BS;
+                const int valid = min(C::BS, u.tok1 - tile0);
+                cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, tile0, p.scale_log2, lane, sm.pbuf[c]);
                 __syncwarp();
                 if (lane == 0) {
                     sm.consumed[stage] += 1;

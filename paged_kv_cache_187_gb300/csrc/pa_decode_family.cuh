@@ -36,22 +36,29 @@ constexpr int stages_for() {
 #define PA_FP8_CORE_CONSUMERS 3
 #endif
 
-template <bool MMA, int BS, bool KV8>
+// Multi-query kernels: up to 16 query rows per unit, twice the tensor-core work per
+// tile of a group-8 decode.
+#ifndef PA_MQ_CONSUMERS
+#define PA_MQ_CONSUMERS(BS) 2
+#endif
+
+template <bool MMA, int BS, bool KV8, bool MQ = false>
 constexpr int consumers_for() {
     // fp8 tiles carry twice the tokens per byte: their consumers do about four times the
     // work per byte of a 16-bit tile, so they get more warps (measured: 4 on the
     // tensor-core path, 3 on the CUDA-core path).
     if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS : PA_FP8_CORE_CONSUMERS;
+    if (MQ) return PA_MQ_CONSUMERS(BS);
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
 
-template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false>
+template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false, bool MQ = false>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
-    constexpr int kCons = consumers_for<MMA, BS, KV8>();
+    constexpr int kCons = consumers_for<MMA, BS, KV8, MQ>();
     using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D * (KV8 ? 1 : 2) / 2, BS, kCons>(), 2,
-                        kCons, KV8>;
+                        kCons, KV8, MQ>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
     static bool configured = false;   // per instantiation; attribute setting is idempotent
@@ -103,6 +110,27 @@ cudaError_t launch_family(const KernelKey& k, const CUtensorMap& kmap, const CUt
     PA_CASE(32, false, 2)
     PA_CASE(32, false, 4)
     PA_CASE(32, false, 8)
+#undef PA_CASE
+    return cudaErrorInvalidValue;
+}
+
+// Multi-query kernels of one dtype: both head sizes, both block sizes, 8 or 16 rows.
+template <bool BF16>
+cudaError_t launch_mq_family(const KernelKey& k, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const DecodeParams& p, bool persistent, int32_t num_units,
+                             cudaStream_t stream, int32_t* occ) {
+#define PA_CASE(D_, BS_, H_)                                                               \
+    if (k.head_size == D_ && k.block_size == BS_ && k.heads_cap == H_)                     \
+        return launch_one<D_, BS_, BF16, true, H_, false, true>(kmap, vmap, p, persistent, \
+                                                               num_units, stream, occ);
+    PA_CASE(128, 16, 8)
+    PA_CASE(128, 16, 16)
+    PA_CASE(128, 32, 8)
+    PA_CASE(128, 32, 16)
+    PA_CASE(64, 16, 8)
+    PA_CASE(64, 16, 16)
+    PA_CASE(64, 32, 8)
+    PA_CASE(64, 32, 16)
 #undef PA_CASE
     return cudaErrorInvalidValue;
 }

@@ -76,6 +76,9 @@ pa_status current_device(int* dev, DeviceInfo* info) {
 cudaError_t dispatch_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
                             const pa::DecodeParams& p, bool persistent, int32_t units,
                             cudaStream_t st, int32_t* occ) {
+    if (k.mq)
+        return k.bf16 ? pa::launch_decode_mq_bf16(k, km, vm, p, persistent, units, st, occ)
+                      : pa::launch_decode_mq_f16(k, km, vm, p, persistent, units, st, occ);
     if (k.kv8)
         return k.bf16 ? pa::launch_decode_fp8kv_bf16q(k, km, vm, p, persistent, units, st, occ)
                       : pa::launch_decode_fp8kv_f16q(k, km, vm, p, persistent, units, st, occ);
@@ -100,7 +103,8 @@ cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CU
 }
 
 int32_t ctas_per_sm(int dev, const pa::KernelKey& k) {
-    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.kv8 << 21 | (uint64_t)(k.head_size == 128) << 20 |
+    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.mq << 22 | (uint64_t)k.kv8 << 21 |
+                         (uint64_t)(k.head_size == 128) << 20 |
                          (uint64_t)(k.block_size == 32) << 19 | (uint64_t)k.bf16 << 18 |
                          (uint64_t)k.mma << 17 | (uint64_t)k.heads_cap;
     {
@@ -176,7 +180,13 @@ struct DecodeArgs {
     cudaStream_t stream;
     bool kv8 = false;      // cache in fp8 E4M3, dequantised by k_scale / v_scale
     float k_scale = 1.f, v_scale = 1.f;
+    int32_t q_len = 1;     // query tokens per sequence (> 1: multi-query kernels)
 };
+
+// Query rows per unit of the multi-query kernels (their head capacity), and the chunks
+// the q_len * group rows of a (sequence, kv head) are split into.
+int32_t mq_heads_cap(int32_t rows) { return rows <= 8 ? 8 : 16; }
+int32_t mq_row_chunks(int32_t rows) { return (rows + mq_heads_cap(rows) - 1) / mq_heads_cap(rows); }
 
 pa_status check_decode(const DecodeArgs& a) {
     if (a.num_seqs < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_blocks <= 0 ||
@@ -196,6 +206,9 @@ pa_status check_decode(const DecodeArgs& a) {
     if (a.num_q_heads / a.num_kv_heads > 16)
         return fail(PA_ERR_UNSUPPORTED, "decode: query group %d > 16",
                     a.num_q_heads / a.num_kv_heads);
+    if (a.q_len < 1 || (int64_t)a.q_len * a.num_q_heads > (1 << 20))
+        return fail(PA_ERR_INVALID_ARG, "decode: q_len %d (1 .. 2^20 / num_q_heads)", a.q_len);
+    if (a.q_len > 1 && a.kv8) return fail(PA_ERR_UNSUPPORTED, "decode: multi-query over an fp8 cache");
     const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
     if (rows + (int64_t)a.num_kv_heads * a.block_size > INT32_MAX)
         return fail(PA_ERR_UNSUPPORTED, "decode: pool has more than 2^31 rows");
@@ -215,6 +228,12 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
     k.bf16 = a.dtype == PA_BF16;
     k.kv8 = a.kv8;
     const int g = a.num_q_heads / a.num_kv_heads;
+    if (a.q_len > 1) {
+        k.mq = true;
+        k.mma = true;
+        k.heads_cap = mq_heads_cap(a.q_len * g);
+        return k;
+    }
     k.mma = g >= 2 && (g > 8 || g_gqa_mma);
     if (k.mma) k.heads_cap = g <= 8 ? 8 : 16;
     else k.heads_cap = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
@@ -239,6 +258,9 @@ pa::DecodeParams base_params(const DecodeArgs& a) {
     p.scale_log2 = a.scale * (a.kv8 ? a.k_scale : 1.f) * 1.4426950408889634f;
     p.out_scale = a.kv8 ? a.v_scale : 1.f;
     p.status = a.status;
+    p.q_len = a.q_len;
+    p.rows = a.q_len * p.group;
+    p.row_chunks = a.q_len > 1 ? mq_row_chunks(p.rows) : 1;
     return p;
 }
 
@@ -256,7 +278,7 @@ pa_status run_v1(const DecodeArgs& a) {
     if ((st = make_maps(a, &km, &vm)) != PA_OK) return st;
     pa::DecodeParams p = base_params(a);
     p.partition_size = 0;
-    const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads;
+    const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * p.row_chunks;
     if (units > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "decode_v1: too many (seq, head) units");
     cudaError_t e = timed_decode(kernel_key(a), km, vm, p, false, (int32_t)units, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_v1 launch");
@@ -273,8 +295,10 @@ pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t w
         return fail(PA_ERR_INVALID_ARG, "decode_v2: partition_size %d must be a positive multiple "
                     "of block_size %d", partition_size, a.block_size);
     if (a.num_seqs == 0) return ok();
-    const pa::WorkspaceLayout L = pa::v2_workspace_layout(a.num_seqs, a.num_q_heads, a.head_size,
-                                                          a.max_context_len, partition_size);
+    // partial rows per partition: q_len * num_q_heads
+    const pa::WorkspaceLayout L = pa::v2_workspace_layout(a.num_seqs, a.num_q_heads * a.q_len,
+                                                          a.head_size, a.max_context_len,
+                                                          partition_size);
     if (!ws || ws_bytes < L.total)
         return fail(PA_ERR_WORKSPACE, "decode_v2: workspace of %zu bytes, need %zu", ws_bytes, L.total);
     if (reinterpret_cast<uintptr_t>(ws) & 255u)
@@ -298,7 +322,8 @@ pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t w
     if (per_sm <= 0) return fail(PA_ERR_CUDA, "decode_v2: kernel cannot be resident on this device");
     const int64_t max_parts_per_seq =
         std::max<int64_t>(1, ((int64_t)a.max_context_len + partition_size - 1) / partition_size);
-    const int64_t max_units = (int64_t)a.num_seqs * max_parts_per_seq * a.num_kv_heads;
+    const int64_t max_units = (int64_t)a.num_seqs * max_parts_per_seq * a.num_kv_heads * p.row_chunks;
+    if (max_units > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "decode_v2: too many work units");
     const int32_t grid = (int32_t)std::min<int64_t>((int64_t)per_sm * di.sms, max_units);
     p.grid_ctas = grid;
     cudaError_t e = pa::launch_plan(p, a.stream);
@@ -669,6 +694,50 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, con
     pa_status st = pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
                                        max_context_len, &v, &P);
     if (st != PA_OK) return st;
+    if (v == 1) return run_v1(a);
+    return run_v2(a, P, workspace, workspace_bytes, /*adaptive=*/true);
+}
+
+size_t pa_decode_mq_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                   int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs < 0 || q_len < 1 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+        block_size <= 0 || max_context_len < 0 || partition_size < 0)
+        return 0;
+    if (partition_size == 0) {
+        int32_t v = 0;
+        auto_plan(num_seqs * mq_row_chunks(q_len * std::max(num_q_heads / num_kv_heads, 1)),
+                  num_kv_heads, block_size, max_context_len, &v, &partition_size);
+        if (v == 1) return 0;
+    }
+    return pa::v2_workspace_layout(num_seqs, num_q_heads * q_len, head_size, max_context_len,
+                                   partition_size).total;
+}
+
+pa_status pa_decode_mq(void* out, const void* query, const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t q_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                       int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                       float scale, pa_dtype dtype, int32_t variant, int32_t partition_size,
+                       void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                       pa_stream stream) {
+    DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                 num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    a.q_len = q_len;
+    if (q_len < 1) return fail(PA_ERR_INVALID_ARG, "decode_mq: q_len %d must be >= 1", q_len);
+    if (num_kv_heads <= 0 || num_q_heads <= 0)
+        return fail(PA_ERR_INVALID_ARG, "decode_mq: sizes must be positive");
+    if (variant == 1) return run_v1(a);
+    if (variant == 2) return run_v2(a, partition_size, workspace, workspace_bytes);
+    if (variant != 0) return fail(PA_ERR_INVALID_ARG, "decode_mq: variant must be 0, 1 or 2");
+    // the auto choice, counting each chunk of query rows as a unit of its own
+    int32_t v = 0, P = 0;
+    const int32_t chunks = q_len > 1 ? mq_row_chunks(q_len * std::max(num_q_heads / num_kv_heads, 1)) : 1;
+    if (num_seqs < 0 || block_size <= 0 || max_context_len < 0)
+        return fail(PA_ERR_INVALID_ARG, "decode_mq: bad sizes");
+    auto_plan(num_seqs * chunks, num_kv_heads, block_size, max_context_len, &v, &P);
     if (v == 1) return run_v1(a);
     return run_v2(a, P, workspace, workspace_bytes, /*adaptive=*/true);
 }

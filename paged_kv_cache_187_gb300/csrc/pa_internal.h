@@ -13,15 +13,15 @@ namespace pa {
 // CTAs claim work units from `counter`.
 struct WsHeader {
     uint32_t counter;         // next unclaimed work unit
-    uint32_t total_units;     // partitions * num_kv_heads
+    uint32_t total_units;     // partitions * num_kv_heads * row_chunks
     uint32_t total_parts;     // partitions over all sequences
     uint32_t partition_size;  // tokens per partition used by this call
     uint32_t pad[60];
 };
 
 struct DecodeParams {
-    void* out;                    // [S][Hq][D] of the dtype
-    const void* q;                // [S][Hq][D]
+    void* out;                    // [S][q_len][Hq][D] of the dtype
+    const void* q;                // [S][q_len][Hq][D]
     const int32_t* block_tables;  // [S][max_blocks_per_seq]
     const int32_t* context_lens;  // [S]
     int32_t max_blocks_per_seq;
@@ -40,10 +40,17 @@ struct DecodeParams {
     WsHeader* hdr;
     int4* part_list;              // [parts] work order: (sequence, partition, first partition
                                   // slot of the sequence, clamped context length)
-    int32_t* arrive;              // [S][Hkv] partitions of (sequence, kv head) finished so far
-    float* part_acc;              // [parts][Hq][D] unnormalised partial outputs
-    float2* part_ml;              // [parts][Hq] (running max in base-2 units, exp-sum)
+    int32_t* arrive;              // [S][Hkv][row_chunks] partitions finished so far
+    float* part_acc;              // [parts][Hkv][rows][D] unnormalised partial outputs
+    float2* part_ml;              // [parts][Hkv][rows] (running max in base-2 units, exp-sum)
     int32_t* status;              // optional device error word
+    // Query rows.  A (sequence, kv head) has rows = q_len * group query rows, row
+    // j * group + i being query token j of the sequence and query head kv_head * group + i.
+    // Ordinary decode: q_len 1, rows = group, row_chunks 1.  Multi-query kernels take
+    // the rows in chunks of their head capacity, one work unit per chunk.
+    int32_t q_len;
+    int32_t rows;
+    int32_t row_chunks;
 };
 
 struct WorkspaceLayout {
@@ -61,6 +68,7 @@ struct KernelKey {
     bool kv8;            // cache in fp8 E4M3
     bool mma;            // tensor-core path (group >= 2) or CUDA-core path
     int32_t heads_cap;   // mma: 8 or 16 (n-tiles * 8); CUDA cores: 1, 2, 4 or 8
+    bool mq = false;     // several causal query tokens per sequence (tensor-core path only)
 };
 
 // Launchers return cudaSuccess or the launch error.  `persistent` selects the V2
@@ -105,6 +113,10 @@ cudaError_t launch_decode_fp8kv_f16q(const KernelKey&, const CUtensorMap&, const
                                      const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
 cudaError_t launch_decode_fp8kv_bf16q(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
                                       const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_mq_f16(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                 const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_mq_bf16(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                  const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
                                          void* value_cache, const int32_t* slot_mapping,
                                          int32_t num_tokens, int32_t num_kv_heads,

@@ -51,6 +51,18 @@ def test_workspace_size_is_host_only_and_monotone(pa):
     assert a >= parts * 32 * (128 * 4 + 8)
 
 
+def test_multi_query_workspace_size(pa):
+    # partial rows per partition are q_len * num_q_heads: the same bytes as an ordinary V2
+    # decode with q_len times the query heads
+    assert (pa.pa_decode_mq_workspace_size(64, 4, 32, 8, 128, 16, 4096, 256) ==
+            pa.pa_decode_v2_workspace_size(64, 128, 128, 4096, 256))
+    # 0: the automatic choice (V2 here, whose smallest partition is 256 tokens)
+    assert (pa.pa_decode_mq_workspace_size(64, 4, 32, 8, 128, 16, 4096, 0) ==
+            pa.pa_decode_v2_workspace_size(64, 128, 128, 4096, 256))
+    assert pa.pa_decode_mq_workspace_size(64, 0, 32, 8, 128, 16, 4096, 256) == 0
+    assert pa.pa_decode_mq_workspace_size(64, 2, 32, 0, 128, 16, 4096, 256) == 0
+
+
 def test_auto_plan_choices(pa):
     v, P = pa.pa_decode_auto_plan(256, 40, 40, 128, 16, 32768)
     assert v == 2 and P % 16 == 0 and P > 0

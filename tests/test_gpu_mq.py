@@ -1,0 +1,147 @@
+"""GPU parity for multi-query decode (several causal query tokens per sequence, the
+attention that verifies speculative tokens): every (sequence, token, head) row against
+the oracle's fp64 multi-query decode, over pools the product's reshape_and_cache filled
+and the oracle's reshape_and_cache rebuilt bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle_side import TOL, bits, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
+    import paged_kv_cache_187_gb300 as pa
+    from paged_kv_cache_187_gb300 import workloads as W
+    lens = np.asarray(lens, np.int32)
+    S = lens.size
+    NB = int(np.sum((lens + bs - 1) // bs) * 1.3) + 4
+    maxb = max(int((lens.max() + bs - 1) // bs), 1)
+    prod = pa.PagedAllocator(NB, bs, seed)
+    ref = oracle.Alloc(NB, bs, seed)
+    poison = W.NAN_BITS[dtype]
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    kc = torch.from_numpy(np.full((NB, Hkv, bs, D), poison, np.uint16).view(np.int16)).to(dev).view(tdt)
+    vc = kc.clone()
+    okc = np.full((NB, Hkv, bs, D), poison, np.uint16)
+    ovc = okc.copy()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for s, L in enumerate(lens):
+        L = int(L)
+        prod.pa_alloc_add_seq(s, L)
+        ref.add_seq(s, L)
+        if L == 0:
+            continue
+        slots = prod.pa_alloc_slots(s, 0, L)
+        assert np.array_equal(slots, ref.slots(s, 0, L))
+        k = W.randn_16bit((L, Hkv, D), dtype, seed * 1000 + 2 * s, dev)
+        v = W.randn_16bit((L, Hkv, D), dtype, seed * 1000 + 2 * s + 1, dev)
+        pa.pa_reshape_and_cache(k, v, kc, vc, torch.from_numpy(slots).to(dev), status=status)
+        assert oracle.reshape_and_cache(bits(k), bits(v), okc, ovc, slots, bs) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(bits(kc), okc) and np.array_equal(bits(vc), ovc)
+    tables = prod.pa_alloc_block_tables(np.arange(S), maxb)
+    q = W.randn_16bit((S, QL, Hq, D), dtype, seed * 1000 + 999, dev)
+    return dict(kc=kc, vc=vc, okc=okc, ovc=ovc, tables=tables, lens=lens, q=q)
+
+
+# (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group
+CASES = [
+    ("bf16", 4, 32, 8, 128, 16),   # 16 rows: one 16-row unit (Llama-3-8B heads)
+    ("f16", 2, 32, 8, 128, 32),    # 8 rows, 32-token blocks
+    ("bf16", 5, 8, 8, 64, 16),     # MHA: 5 rows on the tensor cores, head_size 64
+    ("f16", 3, 16, 2, 128, 16),    # 24 rows: chunks of 16 + 8
+    ("bf16", 2, 16, 1, 64, 32),    # 32 rows: two chunks of 16
+    ("f16", 7, 4, 4, 128, 16),     # 7 rows
+]
+
+
+@pytest.mark.parametrize("dtype,QL,Hq,Hkv,D,bs", CASES)
+def test_multi_query_decode_matches_oracle(cuda_device, dtype, QL, Hq, Hkv, D, bs):
+    import paged_kv_cache_187_gb300 as pa
+    # lengths below q_len give zero rows for the earliest query tokens; 0 is an empty context
+    lens = [0, 1, QL - 1, QL, bs - 1, bs, bs + 1, 100, 257, 511, 513, 1500, 3000]
+    lens = [max(L, 0) for L in lens]
+    b = _batch(cuda_device, lens, QL, Hq, Hkv, D, bs, dtype, seed=71 + QL + Hq + bs)
+    scale = D ** -0.5
+    ref = oracle.decode_mq(bits(b["q"]), b["okc"], b["ovc"], b["tables"], b["lens"],
+                           np.float32(scale), dtype)
+    S = len(lens)
+    out = torch.empty_like(b["q"])
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    mcl = int(b["lens"].max())
+    P = 2 * bs
+    ws = torch.empty(max(pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 0),
+                         pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, P), 256),
+                     dtype=torch.uint8, device=cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for variant, psize in (("auto", 0), ("v1", 0), ("v2", P)):
+        out.fill_(5.0)
+        pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                        variant=variant, partition_size=psize, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        err = max_err(bits(out), ref, dtype)
+        assert err <= TOL[dtype], f"{variant}: {err}"
+        # rows with nothing to attend to are exactly zero
+        for s, L in enumerate(lens):
+            for j in range(QL):
+                if L - QL + j + 1 <= 0:
+                    assert not bits(out[s, j]).any(), (variant, s, j)
+
+
+def test_multi_query_q_len_one_is_the_ordinary_decode(cuda_device):
+    import paged_kv_cache_187_gb300 as pa
+    lens = [5, 40, 300, 1000]
+    b = _batch(cuda_device, lens, 1, 32, 8, 128, 16, "bf16", seed=91)
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    out_mq = torch.empty_like(b["q"])
+    out_v1 = torch.empty(b["q"].shape[0], 32, 128, dtype=b["q"].dtype, device=cuda_device)
+    pa.pa_decode_mq(out_mq, b["q"], b["kc"], b["vc"], tables, lens_d, 1000, 0.088, variant="v1")
+    pa.pa_decode_v1(out_v1, b["q"][:, 0].contiguous(), b["kc"], b["vc"], tables, lens_d, 1000, 0.088)
+    torch.cuda.synchronize()
+    assert torch.equal(out_mq[:, 0].view(torch.int16), out_v1.view(torch.int16))
+
+
+def test_multi_query_full_size_llama3_8b_verify(cuda_device):
+    """Llama-3-8B heads (32 query, 8 kv, head_size 128), 16-token blocks, 4 tokens to
+    verify per sequence, 24 sequences with contexts up to 4096: every row against the
+    oracle, through the launch pa_decode_mq picks by itself."""
+    import paged_kv_cache_187_gb300 as pa
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 4097, size=24).astype(np.int32)
+    lens[0], lens[1] = 4096, 3
+    b = _batch(cuda_device, lens, 4, 32, 8, 128, 16, "bf16", seed=93)
+    ref = oracle.decode_mq(bits(b["q"]), b["okc"], b["ovc"], b["tables"], b["lens"],
+                           np.float32(128 ** -0.5), "bf16")
+    S = lens.size
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    ws = torch.empty(max(pa.pa_decode_mq_workspace_size(S, 4, 32, 8, 128, 16, 4096, 0), 256),
+                     dtype=torch.uint8, device=cuda_device)
+    out = torch.empty_like(b["q"])
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, 4096, 128 ** -0.5,
+                    workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert max_err(bits(out), ref, "bf16") <= TOL["bf16"]
+
+
+def test_multi_query_host_errors(cuda_device):
+    import paged_kv_cache_187_gb300 as pa
+    b = _batch(cuda_device, [20], 2, 8, 8, 128, 16, "f16", seed=95)
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    out = torch.empty_like(b["q"])
+    with pytest.raises(pa.PAError):
+        pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, 20, 0.1, variant="v2",
+                        partition_size=24)    # not a multiple of block_size
+    with pytest.raises(pa.PAError):
+        pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, 20, 0.1, variant="v2",
+                        partition_size=32, workspace=None)
