@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         carry_np += tp;
         carry_nf += tf;
     }
-    const int32_t pairs = p.num_seqs * p.num_kv_heads * p.row_chunks;
+    const int32_t pairs = p.num_seqs * p.num_kv_heads * p.row_chunks * p.row_groups;
     for (int32_t i = tid; i < pairs; i += blockDim.x) p.arrive[i] = 0;
     if (tid == 0) {
         p.hdr->total_parts = (uint32_t)parts;

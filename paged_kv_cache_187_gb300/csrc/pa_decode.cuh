@@ -139,7 +139,10 @@ struct DecodeCfg {
     static constexpr int HALVES = D * ELEM / 128;  // 128-byte swizzle spans per row
     static constexpr int TILE_BYTES = D * BS * ELEM;  // one (block, kv head) tile of K or V
     static constexpr int HALF_BYTES = BS * 128;
-    static constexpr int QROWS = HCAP;
+    // multi-query: a unit has up to NCONS row groups of HCAP rows, each finished by its
+    // own consumer
+    static constexpr int OGROUPS = MQ_ ? NCONS_ : 1;
+    static constexpr int QROWS = OGROUPS * HCAP;
     static constexpr int THREADS = 32 * (1 + NCONS);
     // fp8 configurations run 4 consumer warps; cap their registers so that three CTAs
     // (the shared-memory limit) still fit on an SM.
@@ -164,9 +167,9 @@ template <class C>
 struct alignas(1024) DecodeSmem {
     uint8_t kv[C::NSTAGE][2][C::TILE_BYTES];         // stage: K tile then V tile
     alignas(128) uint8_t qbuf[C::NQ][C::QROWS * C::D * 2];
-    alignas(128) float ostage[C::QROWS * C::D];      // output staging (consumer 0)
+    alignas(128) float ostage[C::OGROUPS][C::HCAP * C::D];   // output staging (per row group)
     float xbuf[C::NCONS > 1 ? C::NCONS - 1 : 1][C::NSTATE * 32];  // consumer states to merge
-    alignas(16) float pbuf[C::NCONS][C::QROWS][C::BS];   // CUDA-core path: softmax weights
+    alignas(16) float pbuf[C::NCONS][C::HCAP][C::BS];   // CUDA-core path: softmax weights
     uint64_t full[C::NSTAGE];
     uint64_t empty[C::NSTAGE];
     uint64_t qfull[C::NQ];
@@ -293,7 +296,8 @@ __device__ __forceinline__ void finish_partition(const DecodeParams& p, const Un
     __syncwarp();
     int last = 0;
     if (lane == 0) {
-        const size_t pair = ((size_t)u.seq * p.num_kv_heads + u.kvh) * p.row_chunks + u.row0 / C::HCAP;
+        const size_t pair = ((size_t)u.seq * p.num_kv_heads + u.kvh) * (p.row_chunks * p.row_groups) +
+                            u.row0 / C::HCAP;
         const int t = atomicAdd(&p.arrive[pair], 1);
         last = (t == u.nparts - 1);
     }
@@ -951,10 +955,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Multi-query units with several row groups: every consumer of a row group reads
+    // every tile of the unit, so a stage is freed by row_groups arrivals.
+    const int32_t row_groups = C::kMq ? p.row_groups : 1;
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NSTAGE; ++i) {
             mbar_init(&sm.full[i], 1);
-            mbar_init(&sm.empty[i], 1);
+            mbar_init(&sm.empty[i], (uint32_t)row_groups);
             sm.issued[i] = 0;
             sm.consumed[i] = 0;
         }
@@ -1006,8 +1013,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 int32_t wu = w;
                 if constexpr (C::kMq) {
                     wu = w / RC;
-                    u.row0 = (w - wu * RC) * C::HCAP;
-                    u.nrows = min(C::HCAP, p.rows - u.row0);
+                    u.row0 = (w - wu * RC) * row_groups * C::HCAP;
+                    u.nrows = min(row_groups * C::HCAP, p.rows - u.row0);
                 }
                 u.kvh = wu % Hkv;
                 if (!persistent) {
@@ -1171,6 +1178,13 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             else return __any_sync(0xffffffffu, v);
         };
         Consumer cons;
+        // Tile split and row group of this consumer: the consumers of a row group share
+        // the unit's tiles round robin (ts = 0 .. TS-1); ordinary kernels have one row
+        // group, so TS = NCONS.  NSTAGE is a multiple of TS, so a stage is always used by
+        // the same consumers.
+        const int TS = C::kMq ? C::NCONS / row_groups : C::NCONS;
+        const int rg = C::kMq ? c / TS : 0;
+        const int ts = C::kMq ? c - rg * TS : c;
         uint32_t gtile = 0;   // tiles of all earlier units, counted over every consumer
         for (uint32_t it = 0;; ++it) {
             const uint32_t qs = it % C::NQ, qphase = (it / C::NQ) & 1;
@@ -1180,9 +1194,14 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 sm.abort = 1;
             }
             if (all_agree(!ok || sm.abort != 0)) break;
-            const UnitDesc u = sm.unit[qs];
+            UnitDesc u = sm.unit[qs];
             if (u.seq < 0) break;
-            cons.load_q(sm.qbuf[qs], u.nrows, lane);
+            if constexpr (C::kMq) {   // this consumer's row group
+                u.row0 += rg * C::HCAP;
+                u.nrows = min(C::HCAP, p.rows - u.row0);
+            }
+            const bool has_rows = u.nrows > 0;
+            cons.load_q(sm.qbuf[qs] + rg * C::HCAP * C::D * 2, u.nrows, lane);
             if constexpr (C::kMq) cons.set_limits(p, u, lane);
             __syncwarp();
             if (lane == 0) {
@@ -1192,7 +1211,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             cons.reset();
             const int32_t b0 = u.tok0 / C::BS, b1 = (u.tok1 + C::BS - 1) / C::BS;
             const int32_t ntiles = b1 - b0;
-            for (int32_t j = c; j < ntiles; j += C::NCONS) {
+            for (int32_t j = ts; j < ntiles; j += TS) {
                 const uint32_t k = gtile + (uint32_t)j;
                 const uint32_t stage = k % C::NSTAGE, fphase = (k / C::NSTAGE) & 1;
                 if (warp_sees_abort(sm.abort)) break;
@@ -1205,23 +1224,25 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 }
                 const int tile0 = (b0 + j) * C::BS;
                 const int valid = min(C::BS, u.tok1 - tile0);
-                cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, tile0, p.scale_log2, lane, sm.pbuf[c]);
+                // a row group past the last row only keeps the stage accounting
+                if (has_rows)
+                    cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, tile0, p.scale_log2, lane, sm.pbuf[c]);
                 __syncwarp();
                 if (lane == 0) {
-                    sm.consumed[stage] += 1;
+                    if (rg == 0) sm.consumed[stage] += 1;
                     mbar_arrive(&sm.empty[stage]);
                 }
             }
             gtile += (uint32_t)ntiles;
             if constexpr (C::NCONS > 1) {
-                if (c > 0) cons.export_state(sm.xbuf[c - 1], lane);
+                if (ts > 0) cons.export_state(sm.xbuf[c - 1], lane);
                 (void)consumers_any(false, kConsThreads);   // states are in shared memory
-                if (c == 0) {
-#pragma unroll
-                    for (int o = 1; o < C::NCONS; ++o) cons.merge_state(sm.xbuf[o - 1], lane);
+                if (ts == 0) {
+                    for (int o = 1; o < TS; ++o) cons.merge_state(sm.xbuf[c + o - 1], lane);
                 }
             }
-            if (c == 0 && !warp_sees_abort(sm.abort)) cons.finish(sm.ostage, p, u, lane);
+            if (ts == 0 && has_rows && !warp_sees_abort(sm.abort))
+                cons.finish(sm.ostage[rg], p, u, lane);
             // also frees xbuf for the next unit
             if (all_agree(sm.abort != 0)) break;
         }

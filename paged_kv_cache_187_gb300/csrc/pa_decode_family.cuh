@@ -36,11 +36,6 @@ constexpr int stages_for() {
 #define PA_FP8_CORE_CONSUMERS 3
 #endif
 
-// Multi-query kernels: up to 16 query rows per unit, twice the tensor-core work per
-// tile of a group-8 decode.
-#ifndef PA_MQ_CONSUMERS
-#define PA_MQ_CONSUMERS(BS) 2
-#endif
 
 template <bool MMA, int BS, bool KV8, bool MQ = false>
 constexpr int consumers_for() {
@@ -48,7 +43,8 @@ constexpr int consumers_for() {
     // work per byte of a 16-bit tile, so they get more warps (measured: 4 on the
     // tensor-core path, 3 on the CUDA-core path).
     if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS : PA_FP8_CORE_CONSUMERS;
-    if (MQ) return PA_MQ_CONSUMERS(BS);
+    // multi-query: one consumer per row group (or, with one row group, per tile)
+    if (MQ) return PA_MQ_CONSUMERS;
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
 

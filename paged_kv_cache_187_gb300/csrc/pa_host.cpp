@@ -183,10 +183,17 @@ struct DecodeArgs {
     int32_t q_len = 1;     // query tokens per sequence (> 1: multi-query kernels)
 };
 
-// Query rows per unit of the multi-query kernels (their head capacity), and the chunks
-// the q_len * group rows of a (sequence, kv head) are split into.
+// Multi-query kernels: rows per consumer (the head capacity), row groups per unit (one
+// consumer each, up to PA_MQ_CONSUMERS), and the units (chunks) the q_len * group rows
+// of a (sequence, kv head) are split into.  Each chunk reads the K/V once.
 int32_t mq_heads_cap(int32_t rows) { return rows <= 8 ? 8 : 16; }
-int32_t mq_row_chunks(int32_t rows) { return (rows + mq_heads_cap(rows) - 1) / mq_heads_cap(rows); }
+int32_t mq_row_groups(int32_t rows) {
+    return std::min<int32_t>(PA_MQ_CONSUMERS, (rows + mq_heads_cap(rows) - 1) / mq_heads_cap(rows));
+}
+int32_t mq_row_chunks(int32_t rows) {
+    const int32_t per = mq_row_groups(rows) * mq_heads_cap(rows);
+    return (rows + per - 1) / per;
+}
 
 pa_status check_decode(const DecodeArgs& a) {
     if (a.num_seqs < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_blocks <= 0 ||
@@ -261,6 +268,7 @@ pa::DecodeParams base_params(const DecodeArgs& a) {
     p.q_len = a.q_len;
     p.rows = a.q_len * p.group;
     p.row_chunks = a.q_len > 1 ? mq_row_chunks(p.rows) : 1;
+    p.row_groups = a.q_len > 1 ? mq_row_groups(p.rows) : 1;
     return p;
 }
 

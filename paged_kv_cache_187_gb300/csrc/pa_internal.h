@@ -40,18 +40,25 @@ struct DecodeParams {
     WsHeader* hdr;
     int4* part_list;              // [parts] work order: (sequence, partition, first partition
                                   // slot of the sequence, clamped context length)
-    int32_t* arrive;              // [S][Hkv][row_chunks] partitions finished so far
+    int32_t* arrive;              // [S][Hkv][row_chunks][row_groups] partitions finished so far
     float* part_acc;              // [parts][Hkv][rows][D] unnormalised partial outputs
     float2* part_ml;              // [parts][Hkv][rows] (running max in base-2 units, exp-sum)
     int32_t* status;              // optional device error word
     // Query rows.  A (sequence, kv head) has rows = q_len * group query rows, row
     // j * group + i being query token j of the sequence and query head kv_head * group + i.
-    // Ordinary decode: q_len 1, rows = group, row_chunks 1.  Multi-query kernels take
-    // the rows in chunks of their head capacity, one work unit per chunk.
+    // Ordinary decode: q_len 1, rows = group, row_chunks = row_groups = 1.  Multi-query
+    // kernels give a work unit row_groups * heads_cap rows, row group r (heads_cap rows)
+    // to its own consumer warps, and split the rows into row_chunks such units.
     int32_t q_len;
     int32_t rows;
     int32_t row_chunks;
+    int32_t row_groups;
 };
+
+// Consumer warps of a multi-query CTA: also the most row groups one unit can have.
+#ifndef PA_MQ_CONSUMERS
+#define PA_MQ_CONSUMERS 2
+#endif
 
 struct WorkspaceLayout {
     size_t hdr, part_list, arrive, part_ml, part_acc, total;

@@ -48,14 +48,17 @@ def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
     return dict(kc=kc, vc=vc, okc=okc, ovc=ovc, tables=tables, lens=lens, q=q)
 
 
-# (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group
+# (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group; a unit
+# holds up to two row groups of 8 or 16 rows
 CASES = [
     ("bf16", 4, 32, 8, 128, 16),   # 16 rows: one 16-row unit (Llama-3-8B heads)
     ("f16", 2, 32, 8, 128, 32),    # 8 rows, 32-token blocks
     ("bf16", 5, 8, 8, 64, 16),     # MHA: 5 rows on the tensor cores, head_size 64
-    ("f16", 3, 16, 2, 128, 16),    # 24 rows: chunks of 16 + 8
-    ("bf16", 2, 16, 1, 64, 32),    # 32 rows: two chunks of 16
+    ("f16", 3, 16, 2, 128, 16),    # 24 rows: one unit, row groups of 16 + 8
+    ("bf16", 2, 16, 1, 64, 32),    # 32 rows: one unit, two full row groups
     ("f16", 7, 4, 4, 128, 16),     # 7 rows
+    ("bf16", 5, 16, 2, 128, 16),   # 40 rows: two units, the second with an empty row group
+    ("f16", 8, 8, 1, 64, 32),      # 64 rows: two units of two full row groups
 ]
 
 
