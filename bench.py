@@ -169,6 +169,16 @@ def _barrier(ws):
         dist.barrier()
 
 
+def _job_totals(bytes_step: float, tokens_step: float, ms_total_local: float, steps: int,
+                ws: int, device) -> dict:
+    """Whole-job figures of a weak-scaling run: every rank processed its own replica of
+    the step `steps` times; the job took as long as the slowest rank."""
+    ms_step = _max_over_ranks(ms_total_local, ws, device) / steps
+    return {"ms_per_step": ms_step,
+            "value": ws * bytes_step / (ms_step * 1e-3) / 1e9,
+            "seq_tokens_per_s": ws * tokens_step / (ms_step * 1e-3)}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def time_oracle(r, budget_s: float = 15.0):
     """Times the fp64 oracle (single thread) on whole sequences of the runner's current
@@ -298,16 +308,12 @@ def run_gpu(args):
     pa.pa_set_kernel_events(None, None)
     time.sleep(0.15)
     clocks.stop()
-    ms_total = t_start.elapsed_time(t_stop)
-    ms_total = _max_over_ranks(ms_total, ws, device)
-    ms_step = ms_total / K
+    job = _job_totals(bytes_step, tokens_step, t_start.elapsed_time(t_stop), K, ws, device)
+    ms_step, value, seq_tok_s = job["ms_per_step"], job["value"], job["seq_tokens_per_s"]
     kern_ms = [a.elapsed_time(b) for a, b in ev_k]
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
     torch.cuda.synchronize(device)
     assert int(r.status.item()) == 0, f"device status {int(r.status.item())}"
-
-    value = ws * bytes_step / (ms_step * 1e-3) / 1e9
-    seq_tok_s = ws * tokens_step / (ms_step * 1e-3)
 
     # ---- end-to-end through the public API from pinned host memory
     e2e = run_e2e(args, w, device, rank, pa, W, DecodeRunner)
