@@ -437,14 +437,35 @@ def run_profile_case(args):
     if args.gqa_cuda_cores:
         pa.pa_set_gqa_tensor_cores(False)
     variant = args.variant
+    if args.q_len > 1:
+        # multi-query decode over the same pools: the last q_len tokens of every context
+        # are the new ones, each with its own query rows
+        S, Hq, D = w.num_seqs, w.num_q_heads, w.head_size
+        mcl = r.step_max_context_len()
+        q = W.randn_16bit((S, args.q_len, Hq, D), w.dtype, W.stream_seed(w, "q", 1), r.device)
+        out = torch.empty_like(q)
+        need = pa.pa_decode_mq_workspace_size(S, args.q_len, Hq, w.num_kv_heads, D,
+                                              w.block_size, mcl, args.partition_size or 0)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=r.device)
+
+        def decode():
+            pa.pa_decode_mq(out, q, r.key_cache, r.value_cache, r.block_tables_d,
+                            r.context_lens_d, mcl, w.scale, variant=variant,
+                            partition_size=args.partition_size or 0, workspace=ws,
+                            status=r.status)
+    else:
+        def decode():
+            r.run_decode(variant, partition_size=args.partition_size)
     for _ in range(args.warmup + args.steps):
-        r.run_decode(variant, partition_size=args.partition_size)
+        decode()
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0
     print(json.dumps({"profile_case": w.name, "kv_fp8": bool(args.kv_fp8), "variant": variant,
-                      "steps": args.steps,
+                      "q_len": args.q_len, "steps": args.steps,
                       "warmup": args.warmup, "gqa_cuda_cores": bool(args.gqa_cuda_cores),
-                      "bytes_per_decode": r.kv_bytes()}))
+                      # K/V once, plus q_len query and output rows per (sequence, head)
+                      "bytes_per_decode": r.kv_bytes() + 2 * (args.q_len - 1) * w.num_seqs *
+                      w.num_q_heads * w.head_size * 2}))
 
 
 def main():
@@ -464,6 +485,8 @@ def main():
                     help="profile case: force the CUDA-core path for grouped-query heads")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="profile case: keep the KV pools in fp8 E4M3")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="profile case: multi-query decode with this many query tokens per sequence")
     args = ap.parse_args()
     if args.profile_workload:
         run_profile_case(args)

@@ -45,11 +45,6 @@ namespace pa {
 #define PA_DEVERR_BAD_LEN_ 4
 #define PA_DEVERR_TIMEOUT_ 8
 
-// Resident CTAs per SM the register allocation of 4-consumer fp8 kernels is sized for.
-#ifndef PA_FP8_MIN_CTAS
-#define PA_FP8_MIN_CTAS 3
-#endif
-
 // Tiles of the current unit still to issue when the producer claims the next unit.
 #ifndef PA_CLAIM_LEAD
 #define PA_CLAIM_LEAD 8
@@ -122,7 +117,7 @@ struct UnitDesc {
 };
 
 template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_, int NCONS_,
-          bool KV8_ = false, bool MQ_ = false>
+          bool KV8_ = false, bool MQ_ = false, int MINB_ = 0>
 struct DecodeCfg {
     static constexpr int D = D_;
     static constexpr int BS = BS_;
@@ -144,9 +139,9 @@ struct DecodeCfg {
     static constexpr int OGROUPS = MQ_ ? NCONS_ : 1;
     static constexpr int QROWS = OGROUPS * HCAP;
     static constexpr int THREADS = 32 * (1 + NCONS);
-    // fp8 configurations run 4 consumer warps; cap their registers so that three CTAs
-    // (the shared-memory limit) still fit on an SM.
-    static constexpr int MIN_CTAS = (KV8_ && NCONS >= 4) ? PA_FP8_MIN_CTAS : 1;
+    // Resident CTAs per SM the register allocation is sized for; 0 leaves the choice to
+    // the compiler (see decode_min_ctas).
+    static constexpr int MIN_CTAS = MINB_;
     // per-lane floats of one consumer's softmax state (m, l, acc)
     static constexpr int NSTATE = MMA_ ? (4 * NT + (D / 16) * NT * 4) : (2 * HCAP_ + HCAP_ * (D / 32));
     static_assert(D == 64 || D == 128, "head_size");

@@ -37,6 +37,33 @@ constexpr int stages_for() {
 #endif
 
 
+// Register budget.  The register file of an SM is four 16K-register quarters, one per
+// scheduler, and a warp's registers come from one quarter: n CTAs of W warps leave a
+// thread 16384 / (32 * ceil(n W / 4)) registers.  Left to itself (no minimum CTA count
+// in the launch bounds) the compiler keeps the 16-bit decode kernels compact enough for
+// the CTAs their shared memory admits; a minimum given explicitly makes it spend
+// registers up to that bound.  The fp8 kernels with 4 consumer warps get one:
+// PA_FP8_MIN_CTAS (3: 15 warps, 128 registers a thread) where the shared memory admits
+// that many -- their consumers are the bottleneck, and the extra warps beat the spills.
+#ifndef PA_FP8_MIN_CTAS
+#define PA_FP8_MIN_CTAS 3
+#endif
+
+// Multi-query kernels with 16-row groups are bound by their tensor-core work; with
+// PA_MQ_MIN_CTAS (2, all their shared memory admits) the compiler gives them the full 255
+// registers, which measured faster than the compact default.  8-row groups do best left
+// to the compiler.
+#ifndef PA_MQ_MIN_CTAS
+#define PA_MQ_MIN_CTAS 2
+#endif
+
+template <class C0>
+constexpr int decode_min_ctas() {
+    constexpr int by_smem = (int)((228 * 1024) / (decode_smem_bytes<C0>() + 1024));
+    if (C0::kMq) return (C0::HCAP == 16 && by_smem >= PA_MQ_MIN_CTAS) ? PA_MQ_MIN_CTAS : 0;
+    return (C0::kKv8 && C0::NCONS >= 4 && by_smem >= PA_FP8_MIN_CTAS) ? PA_FP8_MIN_CTAS : 0;
+}
+
 template <bool MMA, int BS, bool KV8, bool MQ = false>
 constexpr int consumers_for() {
     // fp8 tiles carry twice the tokens per byte: their consumers do about four times the
@@ -53,8 +80,9 @@ cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
     constexpr int kCons = consumers_for<MMA, BS, KV8, MQ>();
-    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, stages_for<D * (KV8 ? 1 : 2) / 2, BS, kCons>(), 2,
-                        kCons, KV8, MQ>;
+    constexpr int kStages = stages_for<D * (KV8 ? 1 : 2) / 2, BS, kCons>();
+    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ,
+                        decode_min_ctas<DecodeCfg<D, BS, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ>>()>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
     static bool configured = false;   // per instantiation; attribute setting is idempotent
