@@ -50,10 +50,16 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# The sources that decide what the measured decode kernel (bf16, head_size 128) does and
+# how it is launched: the kernel, its instantiation, the plan kernel and the host side.
+KERNEL_SOURCES = ("pa_decode.cuh", "pa_decode_family.cuh", "pa_device.cuh", "pa_internal.h",
+                  "pa_decode_bf16_d128.cu", "pa_aux.cu", "pa_host.cpp")
+
+
 def _kernel_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_187_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
