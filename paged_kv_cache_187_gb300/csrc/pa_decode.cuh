@@ -136,8 +136,7 @@ struct DecodeCfg {
     static constexpr int HALF_BYTES = BS * 128;
     // multi-query: a unit has up to NCONS row groups of HCAP rows, each finished by its
     // own consumer
-    static constexpr int OGROUPS = MQ_ ? NCONS_ : 1;
-    static constexpr int QROWS = OGROUPS * HCAP;
+    static constexpr int QROWS = (MQ_ ? NCONS_ : 1) * HCAP;
     static constexpr int THREADS = 32 * (1 + NCONS);
     // Resident CTAs per SM the register allocation is sized for; 0 leaves the choice to
     // the compiler (see decode_min_ctas).
@@ -162,9 +161,14 @@ template <class C>
 struct alignas(1024) DecodeSmem {
     uint8_t kv[C::NSTAGE][2][C::TILE_BYTES];         // stage: K tile then V tile
     alignas(128) uint8_t qbuf[C::NQ][C::QROWS * C::D * 2];
-    alignas(128) float ostage[C::OGROUPS][C::HCAP * C::D];   // output staging (per row group)
-    float xbuf[C::NCONS > 1 ? C::NCONS - 1 : 1][C::NSTATE * 32];  // consumer states to merge
-    alignas(16) float pbuf[C::NCONS][C::HCAP][C::BS];   // CUDA-core path: softmax weights
+    // Output staging of consumer 0.  Multi-query kernels stage each row group's output
+    // in its leader's own xbuf slot instead (see the consumer loop).
+    alignas(128) float ostage[C::kMq ? 1 : C::HCAP * C::D];
+    // Consumer c > 0 exports its softmax state to slot c - 1 for merging; multi-query
+    // kernels have one slot per consumer.
+    alignas(16) float xbuf[C::kMq ? C::NCONS : (C::NCONS > 1 ? C::NCONS - 1 : 1)][C::NSTATE * 32];
+    // CUDA-core path: softmax weights
+    alignas(16) float pbuf[C::kMma ? 1 : C::NCONS][C::kMma ? 1 : C::HCAP][C::kMma ? 1 : C::BS];
     uint64_t full[C::NSTAGE];
     uint64_t empty[C::NSTAGE];
     uint64_t qfull[C::NQ];
@@ -390,7 +394,7 @@ struct MmaConsumer {
     // One tile of BS tokens starting at token tile0, `valid` (1..BS) of which belong to
     // the unit.
     __device__ __forceinline__ void tile(const uint8_t* kt, const uint8_t* vt, int valid, int tile0,
-                                         float scale_log2, int lane, float (*)[BS]) {
+                                         float scale_log2, int lane, const void*) {
         if constexpr (C::kKv8) tile_fp8(kt, vt, valid, scale_log2, lane);
         else tile16(kt, vt, valid, tile0, scale_log2, lane);
     }
@@ -1220,8 +1224,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 const int tile0 = (b0 + j) * C::BS;
                 const int valid = min(C::BS, u.tok1 - tile0);
                 // a row group past the last row only keeps the stage accounting
-                if (has_rows)
-                    cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, tile0, p.scale_log2, lane, sm.pbuf[c]);
+                if (has_rows) {
+                    if constexpr (C::kMma)
+                        cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, tile0, p.scale_log2, lane, nullptr);
+                    else
+                        cons.tile(sm.kv[stage][0], sm.kv[stage][1], valid, tile0, p.scale_log2, lane, sm.pbuf[c]);
+                }
                 __syncwarp();
                 if (lane == 0) {
                     if (rg == 0) sm.consumed[stage] += 1;
@@ -1236,8 +1244,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                     for (int o = 1; o < TS; ++o) cons.merge_state(sm.xbuf[c + o - 1], lane);
                 }
             }
+            // A row group's leader stages its output in its own xbuf slot (multi-query):
+            // that slot belongs to the next consumer of the group, whose state the leader
+            // has just merged, or to no one when the group has one consumer.  The slot
+            // holds NSTATE * 32 >= HCAP * D floats.
             if (ts == 0 && has_rows && !warp_sees_abort(sm.abort))
-                cons.finish(sm.ostage[rg], p, u, lane);
+                cons.finish(C::kMq ? sm.xbuf[c] : sm.ostage, p, u, lane);
             // also frees xbuf for the next unit
             if (all_agree(sm.abort != 0)) break;
         }

@@ -49,14 +49,6 @@ constexpr int stages_for() {
 #define PA_FP8_MIN_CTAS 3
 #endif
 
-// Multi-query kernels with 16-row groups are bound by their tensor-core work; with
-// PA_MQ_MIN_CTAS (2, all their shared memory admits) the compiler gives them the full 255
-// registers, which measured faster than the compact default.  8-row groups do best left
-// to the compiler.
-#ifndef PA_MQ_MIN_CTAS
-#define PA_MQ_MIN_CTAS 2
-#endif
-
 // CUDA-core kernels with one head per unit (MHA): with a minimum of 1 the compiler keeps
 // more K / V rows in flight per lane (about 100 registers instead of 72), measured 1-3 %
 // faster on the MHA workloads; their shared memory, not their registers, still sets the
@@ -65,30 +57,37 @@ constexpr int stages_for() {
 #define PA_CORE_MIN_CTAS 1
 #endif
 
+#ifndef PA_MQ_WIDE_MIN_CTAS
+#define PA_MQ_WIDE_MIN_CTAS 2
+#endif
+
 template <class C0>
 constexpr int decode_min_ctas() {
     constexpr int by_smem = (int)((228 * 1024) / (decode_smem_bytes<C0>() + 1024));
     if (!C0::kMma) return C0::HCAP == 1 ? PA_CORE_MIN_CTAS : 0;
-    if (C0::kMq) return (C0::HCAP == 16 && by_smem >= PA_MQ_MIN_CTAS) ? PA_MQ_MIN_CTAS : 0;
+    // wide multi-query CTAs (5 warps): sized for the CTAs their shared memory admits
+    if (C0::kMq && C0::NCONS >= 4)
+        return by_smem >= PA_MQ_WIDE_MIN_CTAS ? PA_MQ_WIDE_MIN_CTAS : 0;
     return (C0::kKv8 && C0::NCONS >= 4 && by_smem >= PA_FP8_MIN_CTAS) ? PA_FP8_MIN_CTAS : 0;
 }
 
-template <bool MMA, int BS, bool KV8, bool MQ = false>
+// MQC: consumer warps of a multi-query kernel (kMqConsumersNarrow or kMqConsumersWide).
+template <bool MMA, int BS, bool KV8, int MQC = 0>
 constexpr int consumers_for() {
     // fp8 tiles carry twice the tokens per byte: their consumers do about four times the
     // work per byte of a 16-bit tile, so they get more warps (measured: 4 on the
     // tensor-core path, 3 on the CUDA-core path).
     if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS : PA_FP8_CORE_CONSUMERS;
-    // multi-query: one consumer per row group (or, with one row group, per tile)
-    if (MQ) return PA_MQ_CONSUMERS;
+    if (MQC) return MQC;
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
 
-template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false, bool MQ = false>
+template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false, int MQC = 0>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
-    constexpr int kCons = consumers_for<MMA, BS, KV8, MQ>();
+    constexpr bool MQ = MQC > 0;
+    constexpr int kCons = consumers_for<MMA, BS, KV8, MQC>();
     constexpr int kStages = stages_for<D * (KV8 ? 1 : 2) / 2, BS, kCons>();
     using C = DecodeCfg<D, BS, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ,
                         decode_min_ctas<DecodeCfg<D, BS, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ>>()>;
@@ -147,23 +146,25 @@ cudaError_t launch_family(const KernelKey& k, const CUtensorMap& kmap, const CUt
     return cudaErrorInvalidValue;
 }
 
-// Multi-query kernels of one dtype: both head sizes, both block sizes, 8 or 16 rows.
+// Multi-query kernels of one dtype: both head sizes and block sizes, 8 rows per consumer,
+// 2 or 4 consumer warps.
 template <bool BF16>
 cudaError_t launch_mq_family(const KernelKey& k, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const DecodeParams& p, bool persistent, int32_t num_units,
                              cudaStream_t stream, int32_t* occ) {
-#define PA_CASE(D_, BS_, H_)                                                               \
-    if (k.head_size == D_ && k.block_size == BS_ && k.heads_cap == H_)                     \
-        return launch_one<D_, BS_, BF16, true, H_, false, true>(kmap, vmap, p, persistent, \
-                                                               num_units, stream, occ);
-    PA_CASE(128, 16, 8)
-    PA_CASE(128, 16, 16)
-    PA_CASE(128, 32, 8)
-    PA_CASE(128, 32, 16)
-    PA_CASE(64, 16, 8)
-    PA_CASE(64, 16, 16)
-    PA_CASE(64, 32, 8)
-    PA_CASE(64, 32, 16)
+#define PA_CASE(D_, BS_, NC_)                                                                 \
+    if (k.head_size == D_ && k.block_size == BS_ && k.heads_cap == kMqRowsPerConsumer &&      \
+        k.mq_consumers == NC_)                                                                \
+        return launch_one<D_, BS_, BF16, true, kMqRowsPerConsumer, false, NC_>(               \
+            kmap, vmap, p, persistent, num_units, stream, occ);
+    PA_CASE(128, 16, kMqConsumersNarrow)
+    PA_CASE(128, 32, kMqConsumersNarrow)
+    PA_CASE(64, 16, kMqConsumersNarrow)
+    PA_CASE(64, 32, kMqConsumersNarrow)
+    PA_CASE(128, 16, kMqConsumersWide)
+    PA_CASE(128, 32, kMqConsumersWide)
+    PA_CASE(64, 16, kMqConsumersWide)
+    PA_CASE(64, 32, kMqConsumersWide)
 #undef PA_CASE
     return cudaErrorInvalidValue;
 }

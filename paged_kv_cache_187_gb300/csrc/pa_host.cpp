@@ -103,7 +103,8 @@ cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CU
 }
 
 int32_t ctas_per_sm(int dev, const pa::KernelKey& k) {
-    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.mq << 22 | (uint64_t)k.kv8 << 21 |
+    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.mq_consumers << 24 | (uint64_t)k.mq << 22 |
+                         (uint64_t)k.kv8 << 21 |
                          (uint64_t)(k.head_size == 128) << 20 |
                          (uint64_t)(k.block_size == 32) << 19 | (uint64_t)k.bf16 << 18 |
                          (uint64_t)k.mma << 17 | (uint64_t)k.heads_cap;
@@ -183,12 +184,19 @@ struct DecodeArgs {
     int32_t q_len = 1;     // query tokens per sequence (> 1: multi-query kernels)
 };
 
-// Multi-query kernels: rows per consumer (the head capacity), row groups per unit (one
-// consumer each, up to PA_MQ_CONSUMERS), and the units (chunks) the q_len * group rows
-// of a (sequence, kv head) are split into.  Each chunk reads the K/V once.
-int32_t mq_heads_cap(int32_t rows) { return rows <= 8 ? 8 : 16; }
+// Multi-query kernels: rows per consumer (the head capacity), consumer warps per CTA, row
+// groups per unit (a power of two dividing the consumers, so that the consumers of a
+// group share its tiles evenly), and the units (chunks) the q_len * group rows of a
+// (sequence, kv head) are split into.  Each chunk reads the K/V once.
+int32_t mq_heads_cap(int32_t) { return pa::kMqRowsPerConsumer; }
+int32_t mq_consumers(int32_t rows) {
+    return rows <= pa::kMqRowsPerConsumer ? pa::kMqConsumersNarrow : pa::kMqConsumersWide;
+}
 int32_t mq_row_groups(int32_t rows) {
-    return std::min<int32_t>(PA_MQ_CONSUMERS, (rows + mq_heads_cap(rows) - 1) / mq_heads_cap(rows));
+    const int32_t need = (rows + pa::kMqRowsPerConsumer - 1) / pa::kMqRowsPerConsumer;
+    int32_t g = 1;
+    while (g < need && g < mq_consumers(rows)) g *= 2;
+    return g;
 }
 int32_t mq_row_chunks(int32_t rows) {
     const int32_t per = mq_row_groups(rows) * mq_heads_cap(rows);
@@ -239,6 +247,7 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
         k.mq = true;
         k.mma = true;
         k.heads_cap = mq_heads_cap(a.q_len * g);
+        k.mq_consumers = mq_consumers(a.q_len * g);
         return k;
     }
     k.mma = g >= 2 && (g > 8 || g_gqa_mma);

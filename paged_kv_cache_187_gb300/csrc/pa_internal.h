@@ -55,10 +55,13 @@ struct DecodeParams {
     int32_t row_groups;
 };
 
-// Consumer warps of a multi-query CTA: also the most row groups one unit can have.
-#ifndef PA_MQ_CONSUMERS
-#define PA_MQ_CONSUMERS 2
-#endif
+// Multi-query CTAs: each consumer warp holds 8 rows (one mma n-tile).  Up to 8 rows per
+// kv head, 2 consumer warps share the tiles (3 CTAs per SM); above that, 4 consumer
+// warps (2 CTAs per SM) form up to 4 row groups, so a unit covers up to 32 rows in one
+// K/V pass.
+constexpr int32_t kMqRowsPerConsumer = 8;
+constexpr int32_t kMqConsumersNarrow = 2;
+constexpr int32_t kMqConsumersWide = 4;
 
 struct WorkspaceLayout {
     size_t hdr, part_list, arrive, part_ml, part_acc, total;
@@ -76,6 +79,7 @@ struct KernelKey {
     bool mma;            // tensor-core path (group >= 2) or CUDA-core path
     int32_t heads_cap;   // mma: 8 or 16 (n-tiles * 8); CUDA cores: 1, 2, 4 or 8
     bool mq = false;     // several causal query tokens per sequence (tensor-core path only)
+    int32_t mq_consumers = 0;   // multi-query: consumer warps per CTA (2 or 4)
 };
 
 // Launchers return cudaSuccess or the launch error.  `persistent` selects the V2
