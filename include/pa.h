@@ -216,6 +216,13 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, con
  * `partition_size` tokens per partition.  q_len 1 is an ordinary decode.
  * pa_decode_mq_workspace_size: the workspace for variant 2 with `partition_size`, or for
  * variant 0 when partition_size is 0 (V1 needs none); 0 for bad sizes. */
+/* Selects the multi-query kernel for head_size 128 with 16-bit caches and more than 8
+ * query rows (q_len x group) per kv head: 1 (the default) runs it on the 5th-generation
+ * tensor cores (tcgen05, accumulators in tensor memory), 0 on mma.sync.  Fewer rows, and
+ * fixed V2 partition sizes that are not a multiple of 128 tokens, always take the
+ * mma.sync kernel.  Process-wide; returns PA_OK. */
+pa_status pa_set_mq_tcgen05(int32_t enable);
+
 size_t pa_decode_mq_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                    int32_t max_context_len, int32_t partition_size);

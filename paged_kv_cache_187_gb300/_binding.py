@@ -57,6 +57,7 @@ def _load():
         "pa_last_error": ([], ctypes.c_char_p),
         "pa_version": ([], i32),
         "pa_set_gqa_tensor_cores": ([i32], i32),
+        "pa_set_mq_tcgen05": ([i32], i32),
         "pa_set_kernel_events": ([P, P], i32),
         "pa_selftest_wait_timeout": ([P, ctypes.c_uint32, P], i32),
         "pa_reshape_and_cache": ([P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P], i32),
@@ -469,6 +470,10 @@ def pa_selftest_wait_timeout(status, limit_us: int, stream=None):
 
 def pa_set_gqa_tensor_cores(enable: bool):
     _check(_lib.pa_set_gqa_tensor_cores(1 if enable else 0))
+
+
+def pa_set_mq_tcgen05(enable: bool):
+    _check(_lib.pa_set_mq_tcgen05(1 if enable else 0))
 
 
 # --------------------------------------------------------------------------- allocator

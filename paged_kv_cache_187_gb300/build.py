@@ -27,6 +27,7 @@ SOURCES = [
     "pa_decode_fp8.cu",
     "pa_decode_mq_f16.cu",
     "pa_decode_mq_bf16.cu",
+    "pa_decode_tc.cu",
     "pa_aux.cu",
     "pa_noalloc.cu",
     "pa_host.cpp",

@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
             const unsigned long long work =
                 total_tokens * (unsigned long long)p.num_kv_heads * (unsigned long long)p.row_chunks;
             const unsigned long long want = (unsigned long long)max(p.grid_ctas, 1) * PA_UNITS_PER_CTA;
-            unsigned long long Pa = (work / want / (unsigned)bs) * (unsigned)bs;
+            const unsigned align = (unsigned)max(bs, p.partition_align);
+            unsigned long long Pa = (work / want / align) * align;
             if (Pa > (1ull << 30)) Pa = 1ull << 30;
             P_s = max(p.partition_size, (int32_t)Pa);
         }

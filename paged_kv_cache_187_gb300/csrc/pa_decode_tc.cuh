@@ -1,0 +1,741 @@
+// pa_decode_tc.cuh -- multi-query paged decode on the 5th-generation tensor cores
+// (tcgen05, tensor memory), head_size 128.
+//
+// What it computes: the multi-query decode of pa_decode.cuh ("vLLM Project Update" talk,
+// speculative-decoding part: attention for several query tokens per sequence): for every
+// (sequence s, query token j, query head h) row,
+//     out = sum_t softmax_t(scale * q . k_t) v_t  over t < L - q_len + j + 1,
+// K/V paged through the block table, kv head h / group.
+//
+// With many query rows per kv head (q_len x group >= 16) the decode is a real contraction:
+// a 128-token tile against up to 32 rows costs 2 x 128 x 32 x 128 multiply-adds per K/V
+// byte pair, more than mma.sync sustains at the warps per SM its registers allow.  Here
+// the contraction runs on tcgen05 with the accumulators in tensor memory:
+//   * tile = 128 tokens (128 / block_size paged blocks), gathered by TMA into a K ring and
+//     a V ring of 128-byte-swizzled [2 halves][128 tokens][128 B] stages;
+//   * S^T = K Q^T:  M = 128 tokens, N = RPAD (16 or 32) query rows, K = 128 head dims;
+//     A = the K tile (K-major), B = Q (K-major, staged swizzled by the producer);
+//   * softmax over the tile's tokens: 4 warps, one tensor-memory lane (token) per thread,
+//     column maxima by a transposed warp reduction plus a cross-warp exchange;
+//   * O^T += V^T P^T:  M = 128 head dims, N = RPAD, K = 128 tokens; A = the V tile
+//     (MN-major), B = P^T (K-major, written by the softmax warps as P_hi + P_lo for bf16);
+//     O^T stays in tensor memory and is rescaled there when a row maximum moves.
+// Roles: warp 0 streams tiles (TMA), warp 1 issues the MMAs (one thread), warps 2-5 run
+// the softmax and the epilogue.  Work units are the same (sequence, kv head, partition,
+// row chunk) units as the other decode kernels, claimed from the same plan; partitions
+// are multiples of 128 tokens.  Every wait is bounded; the softmax warps take each abort
+// decision together so that none is left at a named barrier.
+#pragma once
+
+#include "pa_decode.cuh"
+
+namespace pa {
+namespace tc {
+
+constexpr int kTok = 128;              // tokens per tile
+constexpr int kD = 128;                // head size
+constexpr uint32_t kHalf = kTok * 128; // one 64-column half of a 128-row tile, bytes
+constexpr int kSoftThreads = 128;      // the four softmax warps
+constexpr int kBarSoft = 1;            // named barrier of the softmax warps
+constexpr float kSlack = 8.f;          // weights stay <= 2^kSlack against the reference
+
+template <bool BF16_, int BS_, int RPAD_>
+struct TcCfg {
+    static constexpr bool kBf16 = BF16_;
+    static constexpr int BS = BS_;
+    static constexpr int RPAD = RPAD_;            // query rows per unit: N of both MMAs
+    static constexpr int BLOCKS = kTok / BS_;     // paged blocks per tile
+    // K and V ring stages (as deep as shared memory allows).  A K tile must land before
+    // its QK^T can start the tile's chain, so K gets 3 stages to cover the load latency
+    // under full HBM traffic; V, streamed by its own warp, is needed one softmax later.
+    static constexpr int NK = 3, NV = RPAD_ == 16 ? 3 : 2;
+    static constexpr int NQ = 2;                  // unit descriptor slots
+    // P as hi + lo bf16 terms, or one fp16 term.  The terms are stacked along N (rows
+    // n and RPAD + n of P^T), so one PV instruction per k-step reads the V tile once and
+    // accumulates O_hi and O_lo side by side; the epilogue adds them.
+    static constexpr int PSPLIT = BF16_ ? 2 : 1;
+    static constexpr int NPV = PSPLIT * RPAD_;           // N of the PV product
+    static constexpr uint32_t TILE_BYTES = 2 * kHalf;   // K (or V) of one tile: 32 KB
+    static constexpr uint32_t QHALF = RPAD_ * 128;      // one 64-dim half of Q
+    static constexpr uint32_t PHALF = NPV * 128;        // one 64-token half of P^T
+    // warps: 0 K producer (claims units, stages Q), 1 MMA issuer, 2-5 softmax, 6 V producer
+    static constexpr int THREADS = 7 * 32;
+    // tensor memory: S^T double-buffered (2 x RPAD columns), then O^T (NPV columns)
+    static constexpr uint32_t COL_S = 0, COL_O = 2 * RPAD_;
+    static constexpr uint32_t TMEM_COLS = (COL_O + NPV <= 64) ? 64 : 128;
+    static_assert(RPAD_ == 16 || RPAD_ == 32, "rows per unit");
+    static_assert(BS_ == 16 || BS_ == 32, "block size");
+};
+
+template <class C>
+struct alignas(1024) TcSmem {
+    uint8_t k[C::NK][C::TILE_BYTES];
+    uint8_t v[C::NV][C::TILE_BYTES];
+    uint8_t q[2][2 * C::QHALF];              // Q of two consecutive units
+    uint8_t p[2][2 * C::PHALF];              // P^T of two consecutive tiles
+    alignas(16) float red[2][C::RPAD][4];   // per-warp column maxima, by tile parity
+    alignas(16) float lred[C::RPAD][4];     // per-warp column exp-sums (epilogue)
+    uint64_t k_full[C::NK], k_empty[C::NK], v_full[C::NV], v_empty[C::NV];
+    uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t q_full[2], q_empty[2], o_full, o_empty, drain;
+    uint64_t u_full[C::NQ], u_empty[C::NQ];
+    UnitDesc unit[C::NQ];
+    uint32_t k_issued[C::NK], v_issued[C::NV];   // TMA tiles issued per stage (producer)
+    uint32_t k_done[C::NK], v_done[C::NV];       // ... whose MMAs were issued (MMA thread)
+    uint32_t tmem_base;
+    int32_t last_flag;
+    volatile int32_t abort;
+};
+
+template <class C>
+constexpr size_t tc_smem_bytes() {
+    return sizeof(TcSmem<C>) + 1024;
+}
+
+// Byte offset of element (row, col) of a [rows][64] 16-bit block stored as 128-byte rows
+// with the 128B swizzle (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t sw128(int row, int col) {
+    const int byte = col * 2;
+    return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15));
+}
+
+// Lane l ends with the max (sum) over the warp of column l % R of v[0..R).
+template <int R, bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[R], int lane) {
+    auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+    int w = R;
+#pragma unroll
+    for (int s = R / 2; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < R / 2; ++i) {
+            if (i < w / 2) {
+                const float send = up ? v[i] : v[i + w / 2];
+                const float keep = up ? v[i + w / 2] : v[i];
+                v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, s));
+            }
+        }
+        w >>= 1;
+    }
+    float r = v[0];
+#pragma unroll
+    for (int s = R; s < 32; s <<= 1) r = op(r, __shfl_xor_sync(0xffffffffu, r, s));
+    return r;
+}
+
+// Row of `out` / q for query row r of a unit: (query token r / group, head kvh*group + r % group).
+__device__ __forceinline__ size_t mq_out_row(const DecodeParams& p, int32_t seq, int32_t kvh, int r) {
+    const int j = r / p.group;
+    return ((size_t)seq * p.q_len + j) * p.num_q_heads + (size_t)kvh * p.group + (r - j * p.group);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap vmap, const DecodeParams p,
+                           const int32_t persistent, const int32_t num_units_v1) {
+    extern __shared__ uint8_t smem_raw[];
+    TcSmem<C>& sm = *reinterpret_cast<TcSmem<C>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int RPAD = C::RPAD;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NK; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);
+            sm.k_issued[i] = sm.k_done[i] = 0;
+        }
+        for (int i = 0; i < C::NV; ++i) {
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_empty[i], 1);
+            sm.v_issued[i] = sm.v_done[i] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.p_full[i], 4);
+            mbar_init(&sm.pv_done[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+        }
+        mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.o_empty, 4);
+        mbar_init(&sm.drain, 1);
+        for (int i = 0; i < C::NQ; ++i) {
+            mbar_init(&sm.u_full[i], 1);
+            mbar_init(&sm.u_empty[i], 6);   // MMA thread, 4 softmax warps, V producer
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+        prefetch_tensor_map(&kmap);
+        prefetch_tensor_map(&vmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    const uint32_t tmem = sm.tmem_base;
+    grid_dependency_wait();   // the plan / reshape kernel before this one has finished
+
+    const int32_t Hkv = p.num_kv_heads, RC = p.row_chunks, upl = Hkv * RC;
+    // Producers (warps 0 and 6, all lanes): block-table entries first .. first+31 of a
+    // unit's sequence, one per lane; entries at or past `end`, or outside the pool, become a
+    // row past the tensor map (TMA reads zeros there).
+    auto load_chunk = [&](const UnitDesc& u, int32_t first, int32_t end) {
+        int32_t phys = p.num_blocks;
+        if (first + lane < end) {
+            phys = p.block_tables[(size_t)u.seq * p.max_blocks_per_seq + first + lane];
+            if (phys < 0 || phys >= p.num_blocks) {
+                if (u.kvh == 0 && u.row0 == 0) flag_error(p.status, PA_DEVERR_BAD_BLOCK_);
+                phys = p.num_blocks;
+            }
+        }
+        return phys;
+    };
+    // Producers: one tile (BLOCKS paged blocks, both 64-column halves) into stage n % ns of
+    // a ring; block b's entry sits in lane within + b of `chunk`.  Lane 0 posts the expected
+    // bytes, then lane 2b + h copies half h of block b.  False when the wait gave up.
+    auto issue_tile = [&](uint8_t (*ring)[C::TILE_BYTES], uint64_t* full, uint64_t* empty,
+                          uint32_t* issued, uint32_t ns, uint32_t n, const CUtensorMap* map,
+                          int32_t chunk, int32_t within, int32_t kvh) {
+        const uint32_t st = n % ns, ph = ((n / ns) & 1) ^ 1;
+        bool ok = true;
+        if (lane == 0) {
+            ok = mbar_wait(&empty[st], ph);
+            if (ok) {
+                mbar_arrive_expect_tx(&full[st], C::TILE_BYTES);
+                issued[st] += 1;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) return false;
+        __syncwarp();   // the expected bytes are posted before any copy is issued
+        const int b = (lane >> 1) & (C::BLOCKS - 1), h = lane & 1;
+        const int32_t pb = __shfl_sync(0xffffffffu, chunk, within + b);
+        if (lane < 2 * C::BLOCKS) {
+            const int32_t y = (pb * Hkv + kvh) * C::BS;
+            tma_load_2d(ring[st] + h * kHalf + b * C::BS * 128, map, h * 64, y, &full[st],
+                        l2_evict_first_policy());
+        }
+        return true;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ K producer
+        const int32_t total = persistent ? (int32_t)p.hdr->total_units : num_units_v1;
+        const int32_t P = persistent ? (int32_t)p.hdr->partition_size : 0;
+        const int4 kNoEntry = make_int4(0, 0, 0, 0);
+        // Unit w as a descriptor: V1 units from the grid index, V2 units from the plan's
+        // list entry e (sequence, partition, first partition slot, length).
+        auto describe = [&](int32_t w, int4 e) {
+            UnitDesc u;
+            u.seq = -1;
+            u.kvh = u.tok0 = u.tok1 = u.pbase = u.row0 = u.nrows = u.len = 0;
+            u.pslot = -1;
+            u.nparts = 1;
+            u.pad[0] = u.pad[1] = 0;
+            if (w < total) {
+                const int32_t wu = w / RC;
+                u.row0 = (w - wu * RC) * RPAD;
+                u.nrows = min(RPAD, p.rows - u.row0);
+                u.kvh = wu % Hkv;
+                if (!persistent) {
+                    u.seq = wu / Hkv;
+                    u.tok1 = clamped_len(p, u.seq, u.kvh == 0 && u.row0 == 0);
+                    u.len = u.tok1;
+                } else {
+                    u.seq = e.x;
+                    u.tok0 = e.y * P;
+                    u.tok1 = min(u.tok0 + P, e.w);
+                    u.nparts = e.w > 0 ? (e.w + P - 1) / P : 1;
+                    u.pbase = e.z;
+                    u.pslot = u.nparts > 1 ? e.z + e.y : -1;
+                    u.len = e.w;
+                }
+            }
+            return u;
+        };
+        // The next unit is claimed as soon as the current one is published and its list
+        // entry is read after the current unit's first tile, so neither round trip stalls
+        // the tile stream.
+        int32_t w = (int32_t)blockIdx.x;
+        if (persistent) {
+            int32_t claimed = 0;
+            if (lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+            w = __shfl_sync(0xffffffffu, claimed, 0);
+        }
+        int4 e = (persistent && w < total) ? p.part_list[w / upl] : kNoEntry;
+        uint32_t kt = 0;   // tiles issued into the K ring
+        bool ok = true;
+        for (uint32_t it = 0; ok; ++it) {
+            const bool done = w >= total || warp_sees_abort(sm.abort);
+            const UnitDesc u = describe(done ? total : w, e);
+            const uint32_t qs = it % C::NQ, qph = ((it / C::NQ) & 1) ^ 1;
+            if (lane == 0) {
+                ok = mbar_wait(&sm.u_empty[qs], qph);
+                if (ok) {
+                    sm.unit[qs] = u;
+                    mbar_arrive(&sm.u_full[qs]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok || u.seq < 0) break;
+            // Q rows of the unit, staged into its Q buffer (unit parity) in the 128B-swizzled
+            // K-major layout, rows past the unit's zero: loads now, stores after the first
+            // tile's copies are issued.  The buffer's previous unit has finished its QK^T.
+            constexpr int kQChunks = RPAD * 16 / 32;   // 16-byte chunks per lane
+            uint4 qv[kQChunks];
+#pragma unroll
+            for (int i = 0; i < kQChunks; ++i) {
+                const int c = lane + 32 * i, n = c >> 4;
+                qv[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (n < u.nrows)
+                    qv[i] = __ldg(reinterpret_cast<const uint4*>(
+                                      reinterpret_cast<const uint16_t*>(p.q) +
+                                      mq_out_row(p, u.seq, u.kvh, u.row0 + n) * kD) + (c & 15));
+            }
+            bool q_staged = false;
+            auto stage_q = [&]() {
+                const uint32_t qb = it & 1;
+                if (lane == 0) ok = mbar_wait(&sm.q_empty[qb], ((it >> 1) & 1) ^ 1);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (ok) {
+#pragma unroll
+                    for (int i = 0; i < kQChunks; ++i) {
+                        const int c = lane + 32 * i, n = c >> 4, ch = c & 15, h = ch >> 3, cc = ch & 7;
+                        *reinterpret_cast<uint4*>(sm.q[qb] + h * C::QHALF + n * 128 + ((cc ^ (n & 7)) << 4)) = qv[i];
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.q_full[qb]);
+                }
+                q_staged = true;
+            };
+            int32_t claimed = total;
+            if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+            int32_t w_next = total;
+            int4 e_next = kNoEntry;
+            bool have_next = false;
+            auto fetch_next = [&]() {
+                w_next = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : total;
+                e_next = (persistent && w_next < total) ? p.part_list[w_next / upl] : kNoEntry;
+                have_next = true;
+            };
+            const int32_t nb0 = u.tok0 / C::BS, nb1 = (u.tok1 + C::BS - 1) / C::BS;
+            const int32_t ntiles = (u.tok1 - u.tok0 + kTok - 1) / kTok;
+            // block-table chunks of 32 entries, the next one always in flight
+            int32_t chunk = 0;
+            int32_t cur = load_chunk(u, nb0, nb1), nxt = load_chunk(u, nb0 + 32, nb1);
+            for (int32_t j = 0; j < ntiles && ok; ++j) {
+                const int32_t tb = j * C::BLOCKS;    // first block of the tile in the unit
+                if ((tb >> 5) != chunk) {
+                    chunk = tb >> 5;
+                    cur = nxt;
+                    nxt = load_chunk(u, nb0 + 32 * (chunk + 1), nb1);
+                }
+                ok = issue_tile(sm.k, sm.k_full, sm.k_empty, sm.k_issued, C::NK, kt, &kmap, cur,
+                                tb & 31, u.kvh);
+                ++kt;
+                if (j == 0) {
+                    stage_q();
+                    fetch_next();
+                }
+            }
+            if (ok && !q_staged) stage_q();
+            if (!have_next) fetch_next();
+            w = w_next;
+            e = e_next;
+        }
+        if (!ok && lane == 0) {
+            flag_error(p.status, PA_DEVERR_TIMEOUT_);
+            sm.abort = 1;
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ V producer
+        // Follows the units the K producer publishes and streams their V tiles into the V
+        // ring, so that a V stage still held by a PV never delays the next K tile.
+        uint32_t vt = 0;
+        bool ok = true;
+        for (uint32_t it = 0; ok; ++it) {
+            const uint32_t qs = it % C::NQ;
+            ok = mbar_wait_warp(&sm.u_full[qs], (it / C::NQ) & 1);
+            if (!ok) break;
+            const UnitDesc u = sm.unit[qs];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.u_empty[qs]);
+            if (u.seq < 0) break;
+            const int32_t nb0 = u.tok0 / C::BS, nb1 = (u.tok1 + C::BS - 1) / C::BS;
+            const int32_t ntiles = (u.tok1 - u.tok0 + kTok - 1) / kTok;
+            int32_t chunk = 0;
+            int32_t cur = load_chunk(u, nb0, nb1), nxt = load_chunk(u, nb0 + 32, nb1);
+            for (int32_t j = 0; j < ntiles && ok; ++j) {
+                const int32_t tb = j * C::BLOCKS;
+                if ((tb >> 5) != chunk) {
+                    chunk = tb >> 5;
+                    cur = nxt;
+                    nxt = load_chunk(u, nb0 + 32 * (chunk + 1), nb1);
+                }
+                ok = issue_tile(sm.v, sm.v_full, sm.v_empty, sm.v_issued, C::NV, vt, &vmap, cur,
+                                tb & 31, u.kvh);
+                ++vt;
+            }
+        }
+        if (!ok && lane == 0) {
+            flag_error(p.status, PA_DEVERR_TIMEOUT_);
+            sm.abort = 1;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = mma_idesc_f16(C::kBf16, 0, 0, kTok, RPAD);
+            constexpr uint32_t kIdPV = mma_idesc_f16(C::kBf16, 1, 0, kD, C::NPV);
+            uint32_t kt = 0, vt = 0, gt = 0, un = 0;
+            bool ok = true;
+            // P^T V of tile t (global tile index), into O^T.
+            auto pv = [&](uint32_t t, bool first) {
+                const uint32_t b = t & 1;
+                ok = mbar_wait(&sm.p_full[b], (t >> 1) & 1);
+                if (ok && first) ok = mbar_wait(&sm.o_empty, (un & 1) ^ 1);
+                const uint32_t vs = vt % C::NV;
+                if (ok) ok = mbar_wait(&sm.v_full[vs], (vt / C::NV) & 1);
+                if (!ok) return;
+                tmem_fence_after_sync();
+                // descriptors differ from the stage's base only in the start address
+                // (16-byte units, low bits): built once, offset per k-step
+                const uint64_t va = smem_desc_sw128(smem_u32(sm.v[vs]), kHalf, 1024);
+                const uint64_t pb = smem_desc_sw128(smem_u32(sm.p[b]), 16, 1024);
+#pragma unroll
+                for (int i = 0; i < kTok / 16; ++i)
+                    mma_f16_ss(tmem + C::COL_O, va + (uint64_t)(i * (2048 >> 4)),
+                               pb + (uint64_t)(((i >> 2) * C::PHALF + (i & 3) * 32) >> 4), kIdPV,
+                               !(first && i == 0));
+                mma_commit(&sm.v_empty[vs]);
+                mma_commit(&sm.pv_done[b]);
+                sm.v_done[vs] += 1;
+                ++vt;
+            };
+            for (uint32_t it = 0; ok; ++it) {
+                const uint32_t qs = it % C::NQ;
+                ok = mbar_wait(&sm.u_full[qs], (it / C::NQ) & 1);
+                if (!ok) break;
+                const UnitDesc u = sm.unit[qs];
+                mbar_arrive(&sm.u_empty[qs]);
+                if (u.seq < 0) break;
+                ok = mbar_wait(&sm.q_full[un & 1], (un >> 1) & 1);
+                if (!ok) break;
+                const uint64_t qd = smem_desc_sw128(smem_u32(sm.q[un & 1]), 16, 1024);
+                const int32_t ntiles = (u.tok1 - u.tok0 + kTok - 1) / kTok;
+                for (int32_t j = 0; j < ntiles && ok; ++j) {
+                    // this tile's QK^T and the previous tile's PV, in whichever order their
+                    // inputs (K tile; published P^T) arrive
+                    bool pv_prev = j > 0;
+                    const uint32_t ks = kt % C::NK;
+                    const uint32_t kbar = smem_u32(&sm.k_full[ks]), kph = (kt / C::NK) & 1;
+                    const uint64_t t0 = global_timer_ns();
+                    while (pv_prev && !mbar_try_wait(kbar, kph)) {
+                        if (mbar_try_wait(smem_u32(&sm.p_full[(gt - 1) & 1]), ((gt - 1) >> 1) & 1)) {
+                            pv(gt - 1, j == 1);
+                            pv_prev = false;
+                        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            ok = false;
+                        }
+                        if (!ok) break;
+                    }
+                    if (!ok) break;
+                    ok = mbar_wait(&sm.k_full[ks], kph);
+                    if (!ok) break;
+                    tmem_fence_after_sync();
+                    const uint64_t ka = smem_desc_sw128(smem_u32(sm.k[ks]), 16, 1024);
+                    const uint32_t d = tmem + C::COL_S + (gt & 1) * RPAD;
+#pragma unroll
+                    for (int i = 0; i < kD / 16; ++i)
+                        mma_f16_ss(d, ka + (uint64_t)(((i >> 2) * kHalf + (i & 3) * 32) >> 4),
+                                   qd + (uint64_t)(((i >> 2) * C::QHALF + (i & 3) * 32) >> 4), kIdQK,
+                                   i > 0);
+                    mma_commit(&sm.s_full[gt & 1]);
+                    mma_commit(&sm.k_empty[ks]);
+                    sm.k_done[ks] += 1;
+                    ++kt;
+                    if (pv_prev) pv(gt - 1, j == 1);
+                    ++gt;
+                }
+                mma_commit(&sm.q_empty[un & 1]);   // this unit's QK^T are all issued
+                if (ok && ntiles > 0) pv(gt - 1, ntiles == 1);
+                if (!ok) break;
+                mma_commit(&sm.o_full);
+                ++un;
+            }
+            if (!ok) {
+                flag_error(p.status, PA_DEVERR_TIMEOUT_);
+                sm.abort = 1;
+            }
+            // every MMA this thread issued has completed before tensor memory is freed
+            mma_commit(&sm.drain);
+            (void)mbar_wait(&sm.drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int sw = warp - 2;                 // softmax warp 0..3
+        const int quarter = warp & 3;            // its tensor-memory lane quarter
+        const int row = quarter * 32 + lane;     // this thread's lane: a token of S^T, a dim of O^T
+        const int tid = sw * 32 + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint32_t gt = 0, un = 0;
+        // Descriptor of unit `it` (the same in all four warps); false when a wait gave up.
+        auto fetch = [&](uint32_t it, UnitDesc& u) {
+            const uint32_t qs = it % C::NQ;
+            const bool ok = mbar_wait_warp(&sm.u_full[qs], (it / C::NQ) & 1);
+            u.seq = -1;
+            if (ok) {
+                u = sm.unit[qs];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.u_empty[qs]);
+            }
+            return !consumers_any(!ok, kSoftThreads);
+        };
+        UnitDesc u;
+        bool failed = !fetch(0, u);
+        for (; !failed && u.seq >= 0; ++un) {
+            // causal limit of each row: tokens below lim[n] are visible
+            int32_t lim[RPAD];
+            // mref[n]: the reference the row's weights are taken against, p = 2^(x - mref).
+            // It only moves when a score exceeds it by more than kSlack (log2 units), so
+            // weights stay <= 2^kSlack and O^T rarely needs rescaling; the result does not
+            // depend on the reference.  ls: this thread's share of the row's weight sum.
+            float mref[RPAD], ls[RPAD];
+#pragma unroll
+            for (int n = 0; n < RPAD; ++n) {
+                lim[n] = min(u.tok1, u.len - p.q_len + (u.row0 + n) / p.group + 1);
+                mref[n] = -INFINITY;
+                ls[n] = 0.f;
+            }
+            const int32_t ntiles = (u.tok1 - u.tok0 + kTok - 1) / kTok;
+            bool bad = false;   // a wait of this warp gave up
+            for (int32_t j = 0; j < ntiles; ++j, ++gt) {
+                const uint32_t b = gt & 1;
+                const int32_t tile0 = u.tok0 + j * kTok;
+                const int32_t tok = tile0 + row;
+                const bool ok = !bad && mbar_wait_warp(&sm.s_full[b], (gt >> 1) & 1);
+                float x[RPAD];
+                bool need = false;
+                if (ok) {
+                    tmem_fence_after_sync();
+#pragma unroll
+                    for (int h = 0; h < RPAD / 16; ++h) {
+                        float s16[16];
+                        tmem_ld16(taddr + C::COL_S + b * RPAD + 16 * h, s16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) x[16 * h + i] = s16[i];
+                    }
+#pragma unroll
+                    for (int n = 0; n < RPAD; ++n) {
+                        x[n] = tok < lim[n] ? x[n] * p.scale_log2 : -INFINITY;
+                        need |= x[n] > mref[n] + kSlack;
+                    }
+                }
+                // one barrier per tile: abort together, or move the references together
+                if (consumers_any(!ok || need, kSoftThreads)) {
+                    if (consumers_any(!ok, kSoftThreads)) {
+                        failed = true;
+                        break;
+                    }
+                    float cmax[RPAD];
+#pragma unroll
+                    for (int n = 0; n < RPAD; ++n) cmax[n] = x[n];
+                    const float wmax = warp_transpose_reduce<RPAD, true>(cmax, lane);
+                    if (lane < RPAD) sm.red[b][lane][sw] = wmax;
+                    named_bar_sync(kBarSoft, kSoftThreads);
+                    bool rescale = false;
+                    float alpha[RPAD];
+#pragma unroll
+                    for (int n = 0; n < RPAD; ++n) {
+                        const float4 r4 = *reinterpret_cast<const float4*>(sm.red[b][n]);
+                        const float mn = fmaxf(mref[n], fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w)));
+                        alpha[n] = mref[n] == -INFINITY ? 0.f : fast_exp2(mref[n] - mn);
+                        rescale |= (j > 0 && mref[n] != -INFINITY && mn > mref[n]);
+                        ls[n] *= alpha[n];
+                        mref[n] = mn;
+                    }
+                    if (rescale) {
+                        // O^T row (head dim `row`) times alpha per query-row column, once the
+                        // PV of the previous tile has landed
+                        const bool okr = mbar_wait_warp(&sm.pv_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1);
+                        if (okr) {
+                            tmem_fence_after_sync();
+                            // (column c of O^T is row c % RPAD: O_hi, then O_lo)
+#pragma unroll
+                            for (int h = 0; h < C::NPV / 16; ++h) {
+                                float o16[16];
+                                tmem_ld16(taddr + C::COL_O + 16 * h, o16);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) o16[i] *= alpha[(16 * h + i) % RPAD];
+                                tmem_st16(taddr + C::COL_O + 16 * h, o16);
+                            }
+                            tmem_wait_st();
+                        }
+                        bad |= !okr;
+                    }
+                    named_bar_sync(kBarSoft, kSoftThreads);   // red[b] is read by all
+                }
+#pragma unroll
+                for (int n = 0; n < RPAD; ++n) {
+                    // a row that has seen no token yet has no reference: its weights are 0
+                    x[n] = fast_exp2(x[n] - (mref[n] == -INFINITY ? 0.f : mref[n]));
+                    ls[n] += x[n];
+                }
+                // P^T buffer b was last read by the PV of tile gt - 2
+                if (!bad && gt >= 2) bad = !mbar_wait_warp(&sm.pv_done[b], ((gt - 2) >> 1) & 1);
+                // the last tile of a unit may stop inside a block: zero the V rows past the
+                // unit (they may hold anything, NaN included; 0 x NaN must not reach O)
+                const int32_t valid = u.tok1 - tile0;
+                if (!bad && valid < kTok) {
+                    const uint32_t vs = gt % C::NV;
+                    bad = !mbar_wait_warp(&sm.v_full[vs], (gt / C::NV) & 1);
+                    if (!bad && row >= valid) {
+                        // chunk order rotated by row: neighbouring lanes hit different banks
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(sm.v[vs] + h * kHalf + row * 128 +
+                                                          (((c + row) & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                if (bad) continue;   // the next barrier makes the abort uniform
+                // P^T[n][token] (this thread's token column)
+                {
+                    const int kh = row >> 6, col = row & 63;
+#pragma unroll
+                    for (int n = 0; n < RPAD; ++n) {
+                        const uint16_t hi = to16<C::kBf16>(x[n]);
+                        *reinterpret_cast<uint16_t*>(sm.p[b] + kh * C::PHALF + sw128(n, col)) = hi;
+                        if constexpr (C::PSPLIT == 2) {
+                            const float hf = __uint_as_float((uint32_t)hi << 16);
+                            *reinterpret_cast<uint16_t*>(sm.p[b] + kh * C::PHALF + sw128(RPAD + n, col)) =
+                                to16<true>(x[n] - hf);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();   // P^T and zeroed V rows -> the tensor core
+                tmem_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.p_full[b]);
+            }
+            if (!failed && consumers_any(bad, kSoftThreads)) failed = true;
+            if (failed) break;
+            float* const m = mref;
+            UnitDesc nu;
+            // ---- epilogue: O^T column n is query row u.row0 + n; this thread holds dim `row`
+            bool ok = mbar_wait_warp(&sm.o_full, un & 1);
+            float o[RPAD];
+            if (ok) {
+                tmem_fence_after_sync();
+#pragma unroll
+                for (int n = 0; n < RPAD; ++n) o[n] = 0.f;
+#pragma unroll
+                for (int h = 0; h < C::NPV / 16; ++h) {   // O_hi + O_lo
+                    float o16[16];
+                    tmem_ld16(taddr + C::COL_O + 16 * h, o16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[(16 * h + i) % RPAD] += ntiles > 0 ? o16[i] : 0.f;
+                }
+                tmem_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.o_empty);
+                float lsum[RPAD];
+#pragma unroll
+                for (int n = 0; n < RPAD; ++n) lsum[n] = ls[n];
+                const float wsum = warp_transpose_reduce<RPAD, false>(lsum, lane);
+                if (lane < RPAD) sm.lred[lane][sw] = wsum;
+            }
+            if (consumers_any(!ok, kSoftThreads)) {
+                failed = true;
+                break;
+            }
+            const bool final_out = u.pslot < 0;
+#pragma unroll
+            for (int n = 0; n < RPAD; ++n) {
+                const float4 l4 = *reinterpret_cast<const float4*>(sm.lred[n]);
+                const float L = (l4.x + l4.y) + (l4.z + l4.w);
+                if (n < u.nrows) {
+                    if (final_out) {
+                        const float inv = L > 0.f ? p.out_scale / L : 0.f;
+                        reinterpret_cast<uint16_t*>(p.out)[mq_out_row(p, u.seq, u.kvh, u.row0 + n) * kD + row] =
+                            to16<C::kBf16>(o[n] * inv);
+                    } else {
+                        const size_t pr = part_row(p, u, u.pslot, n);
+                        p.part_acc[pr * kD + row] = o[n];
+                        if (tid == 0) p.part_ml[pr] = make_float2(m[n], L);
+                    }
+                }
+            }
+            if (!final_out) {
+                // count this partition; the last of the (sequence, kv head, row chunk)
+                // merges all partials by log-sum-exp
+                __threadfence();
+                named_bar_sync(kBarSoft, kSoftThreads);
+                if (tid == 0) {
+                    const size_t pair = ((size_t)u.seq * Hkv + u.kvh) * (size_t)RC + u.row0 / RPAD;
+                    sm.last_flag = atomicAdd(&p.arrive[pair], 1) == u.nparts - 1;
+                }
+                named_bar_sync(kBarSoft, kSoftThreads);
+                if (sm.last_flag) {
+                    __threadfence();
+                    for (int n = 0; n < u.nrows; ++n) {
+                        float M = -INFINITY, den = 0.f, acc = 0.f;
+                        for (int q = 0; q < u.nparts; ++q) {
+                            const size_t pr = part_row(p, u, u.pbase + q, n);
+                            const float2 ml = __ldcg(&p.part_ml[pr]);
+                            const float a = __ldcg(&p.part_acc[pr * kD + row]);
+                            const float Mn = fmaxf(M, ml.x);
+                            const float f = state_weight(M, Mn), wq = state_weight(ml.x, Mn);
+                            den = den * f + wq * ml.y;
+                            acc = acc * f + wq * a;
+                            M = Mn;
+                        }
+                        const float inv = den > 0.f ? p.out_scale / den : 0.f;
+                        reinterpret_cast<uint16_t*>(p.out)[mq_out_row(p, u.seq, u.kvh, u.row0 + n) * kD + row] =
+                            to16<C::kBf16>(acc * inv);
+                    }
+                }
+            }
+            named_bar_sync(kBarSoft, kSoftThreads);   // lred and last_flag are reused
+            if (!fetch(un + 1, nu)) {
+                failed = true;
+                break;
+            }
+            u = nu;
+        }
+        if (failed && lane == 0) {
+            flag_error(p.status, PA_DEVERR_TIMEOUT_);
+            sm.abort = 1;
+        }
+    }
+
+    // Teardown.  After an abort, copies may still be landing in shared memory: wait
+    // (bounded) for every stage whose TMA was issued but never fed to an MMA.
+    __syncthreads();
+    if (threadIdx.x == 0 && sm.abort) {
+        for (int i = 0; i < C::NK; ++i)
+            if (sm.k_issued[i] > sm.k_done[i]) (void)mbar_wait(&sm.k_full[i], sm.k_done[i] & 1);
+        for (int i = 0; i < C::NV; ++i)
+            if (sm.v_issued[i] > sm.v_done[i]) (void)mbar_wait(&sm.v_full[i], sm.v_done[i] & 1);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tmem_fence_after_sync();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+}  // namespace pa

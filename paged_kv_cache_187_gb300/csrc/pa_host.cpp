@@ -51,6 +51,7 @@ std::mutex g_mu;
 std::unordered_map<int, DeviceInfo> g_dev;
 std::unordered_map<uint64_t, int32_t> g_occ;   // (device, kernel key) -> CTAs per SM
 int32_t g_gqa_mma = 1;
+int32_t g_mq_tc = 1;
 cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 
 // Launches the decode kernel, bracketed by the profiling events when they are set.
@@ -76,6 +77,7 @@ pa_status current_device(int* dev, DeviceInfo* info) {
 cudaError_t dispatch_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
                             const pa::DecodeParams& p, bool persistent, int32_t units,
                             cudaStream_t st, int32_t* occ) {
+    if (k.tc) return pa::launch_decode_mq_tc(k, km, vm, p, persistent, units, st, occ);
     if (k.mq)
         return k.bf16 ? pa::launch_decode_mq_bf16(k, km, vm, p, persistent, units, st, occ)
                       : pa::launch_decode_mq_f16(k, km, vm, p, persistent, units, st, occ);
@@ -103,7 +105,8 @@ cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CU
 }
 
 int32_t ctas_per_sm(int dev, const pa::KernelKey& k) {
-    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.mq_consumers << 24 | (uint64_t)k.mq << 22 |
+    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.tc << 28 | (uint64_t)k.mq_consumers << 24 |
+                         (uint64_t)k.mq << 22 |
                          (uint64_t)k.kv8 << 21 |
                          (uint64_t)(k.head_size == 128) << 20 |
                          (uint64_t)(k.block_size == 32) << 19 | (uint64_t)k.bf16 << 18 |
@@ -182,7 +185,21 @@ struct DecodeArgs {
     bool kv8 = false;      // cache in fp8 E4M3, dequantised by k_scale / v_scale
     float k_scale = 1.f, v_scale = 1.f;
     int32_t q_len = 1;     // query tokens per sequence (> 1: multi-query kernels)
+    int32_t partition_size = 0;   // V2 with a fixed partition size (0: none given)
 };
+
+// The tcgen05 multi-query kernel takes head_size 128, 16-bit caches, and partitions that
+// are multiples of its 128-token tile; it holds 16 or 32 query rows per unit.  It is used
+// from 9 query rows per kv head on: with fewer rows the mma.sync kernel's three CTAs per
+// SM hide the load latency better than its single tile pipeline per SM (measured on the
+// Llama-3-8B / -70B batches: 8 rows 231 vs 197 us; 16 rows 246 vs 266 us and 685 vs
+// 647 us; 32 rows 365 vs 366 us and 924 vs 1034 us).
+bool use_mq_tc(const DecodeArgs& a) {
+    const int32_t rows = a.q_len * (a.num_q_heads / std::max(a.num_kv_heads, 1));
+    return g_mq_tc && a.q_len > 1 && rows > 8 && a.head_size == 128 && !a.kv8 &&
+           (a.partition_size == 0 || a.partition_size % pa::kTcTileTokens == 0);
+}
+int32_t mq_tc_rows(int32_t rows) { return rows <= 16 ? 16 : 32; }
 
 // Multi-query kernels: rows per consumer (the head capacity), consumer warps per CTA, row
 // groups per unit (a power of two dividing the consumers, so that the consumers of a
@@ -246,6 +263,11 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
     if (a.q_len > 1) {
         k.mq = true;
         k.mma = true;
+        if (use_mq_tc(a)) {
+            k.tc = true;
+            k.heads_cap = mq_tc_rows(a.q_len * g);
+            return k;
+        }
         k.heads_cap = mq_heads_cap(a.q_len * g);
         k.mq_consumers = mq_consumers(a.q_len * g);
         return k;
@@ -276,8 +298,15 @@ pa::DecodeParams base_params(const DecodeArgs& a) {
     p.status = a.status;
     p.q_len = a.q_len;
     p.rows = a.q_len * p.group;
-    p.row_chunks = a.q_len > 1 ? mq_row_chunks(p.rows) : 1;
-    p.row_groups = a.q_len > 1 ? mq_row_groups(p.rows) : 1;
+    if (use_mq_tc(a)) {
+        const int32_t r = mq_tc_rows(p.rows);
+        p.row_chunks = (p.rows + r - 1) / r;
+        p.row_groups = 1;
+        p.partition_align = pa::kTcTileTokens;
+    } else {
+        p.row_chunks = a.q_len > 1 ? mq_row_chunks(p.rows) : 1;
+        p.row_groups = a.q_len > 1 ? mq_row_groups(p.rows) : 1;
+    }
     return p;
 }
 
@@ -304,8 +333,10 @@ pa_status run_v1(const DecodeArgs& a) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-pa_status run_v2(const DecodeArgs& a, int32_t partition_size, void* ws, size_t ws_bytes,
+pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_t ws_bytes,
                  bool adaptive = false) {
+    DecodeArgs a = a_in;
+    a.partition_size = adaptive ? 0 : partition_size;
     pa_status st = check_decode(a);
     if (st != PA_OK) return st;
     if (partition_size <= 0 || partition_size % a.block_size)
@@ -564,6 +595,11 @@ pa_status pa_set_kernel_events(void* start_event, void* stop_event) {
 
 pa_status pa_set_gqa_tensor_cores(int32_t enable) {
     g_gqa_mma = enable ? 1 : 0;
+    return ok();
+}
+
+pa_status pa_set_mq_tcgen05(int32_t enable) {
+    g_mq_tc = enable ? 1 : 0;
     return ok();
 }
 

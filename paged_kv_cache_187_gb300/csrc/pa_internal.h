@@ -53,6 +53,7 @@ struct DecodeParams {
     int32_t rows;
     int32_t row_chunks;
     int32_t row_groups;
+    int32_t partition_align;      // V2: partitions are multiples of this many tokens (0: block_size)
 };
 
 // Multi-query CTAs: each consumer warp holds 8 rows (one mma n-tile).  Up to 8 rows per
@@ -80,6 +81,7 @@ struct KernelKey {
     int32_t heads_cap;   // mma: 8 or 16 (n-tiles * 8); CUDA cores: 1, 2, 4 or 8
     bool mq = false;     // several causal query tokens per sequence (tensor-core path only)
     int32_t mq_consumers = 0;   // multi-query: consumer warps per CTA (2 or 4)
+    bool tc = false;            // multi-query on tcgen05 (heads_cap = rows per unit, 16 or 32)
 };
 
 // Launchers return cudaSuccess or the launch error.  `persistent` selects the V2
@@ -128,6 +130,10 @@ cudaError_t launch_decode_mq_f16(const KernelKey&, const CUtensorMap&, const CUt
                                  const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
 cudaError_t launch_decode_mq_bf16(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
                                   const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+cudaError_t launch_decode_mq_tc(const KernelKey&, const CUtensorMap&, const CUtensorMap&,
+                                const DecodeParams&, bool, int32_t, cudaStream_t, int32_t*);
+// Tokens per tile of the tcgen05 multi-query kernel (its partitions are multiples of it).
+constexpr int32_t kTcTileTokens = 128;
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
                                          void* value_cache, const int32_t* slot_mapping,
                                          int32_t num_tokens, int32_t num_kv_heads,

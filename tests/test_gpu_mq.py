@@ -12,6 +12,15 @@ from oracle_side import TOL, bits, max_err
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=[True, False], ids=["tcgen05", "mma_sync"])
+def mq_kernel(request, cuda_device):
+    """Runs a test with the tcgen05 multi-query kernel (head_size 128) or the mma.sync one."""
+    import paged_kv_cache_187_gb300 as pa
+    pa.pa_set_mq_tcgen05(request.param)
+    yield request.param
+    pa.pa_set_mq_tcgen05(True)
+
+
 def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
     import paged_kv_cache_187_gb300 as pa
     from paged_kv_cache_187_gb300 import workloads as W
@@ -48,8 +57,10 @@ def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
     return dict(kc=kc, vc=vc, okc=okc, ovc=ovc, tables=tables, lens=lens, q=q)
 
 
-# (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group; a unit
-# holds up to two row groups of 8 or 16 rows
+# (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group.  With
+# head_size 128 and more than 8 rows the tcgen05 kernel takes the case (16 or 32 rows per
+# unit) unless the test switches it off; otherwise the mma.sync kernel (up to 4 row groups
+# of 8 rows per unit).
 CASES = [
     ("bf16", 4, 32, 8, 128, 16),   # 16 rows: one 16-row unit (Llama-3-8B heads)
     ("f16", 2, 32, 8, 128, 32),    # 8 rows, 32-token blocks
@@ -59,11 +70,13 @@ CASES = [
     ("f16", 7, 4, 4, 128, 16),     # 7 rows
     ("bf16", 5, 16, 2, 128, 16),   # 40 rows: two units, the second with an empty row group
     ("f16", 8, 8, 1, 64, 32),      # 64 rows: two units of two full row groups
+    ("f16", 4, 16, 2, 128, 32),    # 32 rows, 32-token blocks
+    ("bf16", 3, 32, 8, 128, 32),   # 12 rows, 32-token blocks
 ]
 
 
 @pytest.mark.parametrize("dtype,QL,Hq,Hkv,D,bs", CASES)
-def test_multi_query_decode_matches_oracle(cuda_device, dtype, QL, Hq, Hkv, D, bs):
+def test_multi_query_decode_matches_oracle(cuda_device, mq_kernel, dtype, QL, Hq, Hkv, D, bs):
     import paged_kv_cache_187_gb300 as pa
     # lengths below q_len give zero rows for the earliest query tokens; 0 is an empty context
     lens = [0, 1, QL - 1, QL, bs - 1, bs, bs + 1, 100, 257, 511, 513, 1500, 3000]
@@ -77,12 +90,12 @@ def test_multi_query_decode_matches_oracle(cuda_device, dtype, QL, Hq, Hkv, D, b
     tables = torch.from_numpy(b["tables"]).to(cuda_device)
     lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
     mcl = int(b["lens"].max())
-    P = 2 * bs
+    # 128-token partitions suit both kernels; 2 x block_size ones only the mma.sync kernel
     ws = torch.empty(max(pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 0),
-                         pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, P), 256),
+                         pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 2 * bs), 256),
                      dtype=torch.uint8, device=cuda_device)
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    for variant, psize in (("auto", 0), ("v1", 0), ("v2", P)):
+    for variant, psize in (("auto", 0), ("v1", 0), ("v2", 128), ("v2", 2 * bs)):
         out.fill_(5.0)
         pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, mcl, scale,
                         variant=variant, partition_size=psize, workspace=ws, status=status)
@@ -111,7 +124,7 @@ def test_multi_query_q_len_one_is_the_ordinary_decode(cuda_device):
     assert torch.equal(out_mq[:, 0].view(torch.int16), out_v1.view(torch.int16))
 
 
-def test_multi_query_full_size_llama3_8b_verify(cuda_device):
+def test_multi_query_full_size_llama3_8b_verify(cuda_device, mq_kernel):
     """Llama-3-8B heads (32 query, 8 kv, head_size 128), 16-token blocks, 4 tokens to
     verify per sequence, 24 sequences with contexts up to 4096: every row against the
     oracle, through the launch pa_decode_mq picks by itself."""
