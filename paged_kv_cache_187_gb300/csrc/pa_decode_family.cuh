@@ -30,7 +30,7 @@ constexpr int stages_for() {
 // Consumer warps per CTA: the CUDA-core path needs more warps to keep up with HBM than
 // the tensor-core path does.
 #ifndef PA_FP8_MMA_CONSUMERS
-#define PA_FP8_MMA_CONSUMERS 4
+#define PA_FP8_MMA_CONSUMERS(BS) ((BS) == 16 ? 2 : 3)
 #endif
 #ifndef PA_FP8_CORE_CONSUMERS
 #define PA_FP8_CORE_CONSUMERS 3
@@ -40,23 +40,19 @@ constexpr int stages_for() {
 // Register budget.  The register file of an SM is four 16K-register quarters, one per
 // scheduler, and a warp's registers come from one quarter: n CTAs of W warps leave a
 // thread 16384 / (32 * ceil(n W / 4)) registers.  Left to itself (no minimum CTA count
-// in the launch bounds) the compiler keeps the 16-bit decode kernels compact enough for
-// the CTAs their shared memory admits; a minimum given explicitly makes it spend
-// registers up to that bound.  The fp8 kernels with 4 consumer warps get one:
-// PA_FP8_MIN_CTAS (3: 15 warps, 128 registers a thread) where the shared memory admits
-// that many -- their consumers are the bottleneck, and the extra warps beat the spills.
-#ifndef PA_FP8_MIN_CTAS
-#define PA_FP8_MIN_CTAS 3
-#endif
-
-// CUDA-core kernels with one head per unit (MHA): with a minimum of 1 the compiler keeps
-// more K / V rows in flight per lane (about 100 registers instead of 72), measured 1-3 %
-// faster on the MHA workloads; their shared memory, not their registers, still sets the
-// CTAs per SM.  (With more heads the same bound would cost those kernels a CTA.)
+// in the launch bounds) the compiler keeps the tensor-core decode kernels compact enough
+// for the CTAs their shared memory admits (144 registers for the GQA and fp8 kernels); a
+// minimum given explicitly makes it spend registers up to that bound.  Two kinds carry
+// one, each measured faster:
+//   * CUDA-core kernels with one head per unit (MHA): a minimum of 1 lets the compiler
+//     keep more K / V rows in flight per lane (about 100 registers instead of 72), 1-3 %
+//     on the MHA workloads; their shared memory still sets the CTAs per SM.  (With more
+//     heads the same bound would cost those kernels a CTA.)
+//   * 4-consumer multi-query kernels (5 warps): sized for the 2 CTAs their shared memory
+//     admits (168 registers instead of the compiler's 128 with spills).
 #ifndef PA_CORE_MIN_CTAS
 #define PA_CORE_MIN_CTAS 1
 #endif
-
 #ifndef PA_MQ_WIDE_MIN_CTAS
 #define PA_MQ_WIDE_MIN_CTAS 2
 #endif
@@ -65,19 +61,19 @@ template <class C0>
 constexpr int decode_min_ctas() {
     constexpr int by_smem = (int)((228 * 1024) / (decode_smem_bytes<C0>() + 1024));
     if (!C0::kMma) return C0::HCAP == 1 ? PA_CORE_MIN_CTAS : 0;
-    // wide multi-query CTAs (5 warps): sized for the CTAs their shared memory admits
     if (C0::kMq && C0::NCONS >= 4)
         return by_smem >= PA_MQ_WIDE_MIN_CTAS ? PA_MQ_WIDE_MIN_CTAS : 0;
-    return (C0::kKv8 && C0::NCONS >= 4 && by_smem >= PA_FP8_MIN_CTAS) ? PA_FP8_MIN_CTAS : 0;
+    return 0;
 }
 
 // MQC: consumer warps of a multi-query kernel (kMqConsumersNarrow or kMqConsumersWide).
 template <bool MMA, int BS, bool KV8, int MQC = 0>
 constexpr int consumers_for() {
-    // fp8 tiles carry twice the tokens per byte: their consumers do about four times the
-    // work per byte of a 16-bit tile, so they get more warps (measured: 4 on the
-    // tensor-core path, 3 on the CUDA-core path).
-    if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS : PA_FP8_CORE_CONSUMERS;
+    // fp8 tiles carry twice the tokens per byte, so their consumers do about four times
+    // the work per byte of a 16-bit tile.  Measured on the Llama-3-8B / -70B batches, the
+    // tensor-core path does best with 2 consumer warps for 16-token blocks (4 CTAs per SM
+    // at 144 registers) and 3 for 32-token blocks; the CUDA-core path with 3.
+    if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS(BS) : PA_FP8_CORE_CONSUMERS;
     if (MQC) return MQC;
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
