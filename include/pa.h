@@ -211,18 +211,11 @@ pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, con
  *   query, out  [num_seqs][q_len][num_q_heads][head_size], fp16 or bf16 (`dtype`, also
  *               the cache type); other arguments as for pa_decode_v1 / pa_decode_v2.
  * The q_len * group rows of a (sequence, kv head) share one pass over its K/V on the
- * tensor cores, 16 rows at a time (more rows re-read the K/V once per 16).  variant 0 =
+ * tensor cores, up to 32 rows at a time (more rows re-read the K/V once per 32).  variant 0 =
  * pa_decode_auto's choice (V1 or V2 with adaptive partitions), 1 = V1, 2 = V2 with
  * `partition_size` tokens per partition.  q_len 1 is an ordinary decode.
  * pa_decode_mq_workspace_size: the workspace for variant 2 with `partition_size`, or for
  * variant 0 when partition_size is 0 (V1 needs none); 0 for bad sizes. */
-/* Selects the multi-query kernel for head_size 128 with 16-bit caches and more than 8
- * query rows (q_len x group) per kv head: 1 (the default) runs it on the 5th-generation
- * tensor cores (tcgen05, accumulators in tensor memory), 0 on mma.sync.  Fewer rows, and
- * fixed V2 partition sizes that are not a multiple of 128 tokens, always take the
- * mma.sync kernel.  Process-wide; returns PA_OK. */
-pa_status pa_set_mq_tcgen05(int32_t enable);
-
 size_t pa_decode_mq_workspace_size(int32_t num_seqs, int32_t q_len, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                    int32_t max_context_len, int32_t partition_size);
@@ -234,6 +227,13 @@ pa_status pa_decode_mq(void* out, const void* query, const void* key_cache, cons
                        float scale, pa_dtype dtype, int32_t variant, int32_t partition_size,
                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
                        pa_stream stream);
+
+/* Selects the multi-query kernel for head_size 128 with 16-bit caches and more than 8
+ * query rows (q_len x group) per kv head: 1 (the default) runs it on the 5th-generation
+ * tensor cores (tcgen05, accumulators in tensor memory), 0 on mma.sync.  Fewer rows, and
+ * fixed V2 partition sizes that are not a multiple of 128 tokens, always take the
+ * mma.sync kernel.  Process-wide; returns PA_OK. */
+pa_status pa_set_mq_tcgen05(int32_t enable);
 
 /* One decode step of the hot path on device buffers: pa_reshape_and_cache of the
  * step's new K/V rows, then pa_decode_auto, on the same stream. */
