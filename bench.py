@@ -368,10 +368,10 @@ def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
     """Serving loop through the public C ABI from host memory, pipelined the way a
     server runs it: while the GPU runs step i, the host allocator appends step i+1's
     tokens and writes its slots / block tables / lengths straight into the next slot of
-    a ring of pinned buffers, and pa_decode_step_host queues step i+1 (H2D of its
-    q/k/v/metadata, reshape_and_cache + decode, D2H of out).  Before a ring slot is
-    reused, the host waits for that step's output to have arrived in host memory.  Every
-    step's copies lie inside the timed region."""
+    a ring of pinned buffers, and pa_decode_step_host_overlapped queues step i+1 (H2D of
+    its q/k/v/metadata on an H2D stream, reshape_and_cache + decode on the compute stream,
+    D2H of out on a D2H stream), so that a step's copies overlap its neighbours' kernels.  Before a ring slot is reused, the host waits for that step's output to have
+    arrived in host memory.  Every step's copies lie inside the timed region."""
     import dataclasses
     import torch
     K = min(args.steps, args.e2e_steps)
@@ -388,10 +388,16 @@ def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
     lens_h = [torch.empty(S, dtype=torch.int32).pin_memory() for _ in range(ring)]
     tables_h = [torch.empty((S, r.max_blocks), dtype=torch.int32).pin_memory() for _ in range(ring)]
     out_h = [torch.empty((S, Hq, D), dtype=tdt).pin_memory() for _ in range(ring)]
+    # per ring slot: staging area, copies-landed / step-done / output-back events
+    ssize = pa.pa_decode_step_host_staging_size(S, Hq, Hkv, D, r.max_blocks)
+    staging = [torch.empty(ssize, dtype=torch.uint8, device=device) for _ in range(ring)]
+    h2d_stream = torch.cuda.Stream(device)
+    d2h_stream = torch.cuda.Stream(device)
+    staged = [torch.cuda.Event() for _ in range(ring)]
+    stepped = [torch.cuda.Event() for _ in range(ring)]
     done = [torch.cuda.Event() for _ in range(ring)]
-    # one staging area suffices: the stream runs the steps in order
-    staging = torch.empty(pa.pa_decode_step_host_staging_size(S, Hq, Hkv, D, r.max_blocks),
-                          dtype=torch.uint8, device=device)
+    for e in staged + stepped + done:
+        e.record(d2h_stream)           # the CUDA events exist from here on
     need = pa.pa_decode_auto_workspace_size(S, Hq, Hkv, D, w.block_size,
                                             r.max_context_len + K + warm)
     if need > r.workspace.numel():
@@ -420,10 +426,11 @@ def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
         lens_np = lens_h[j].numpy()
         r.alloc.pa_alloc_context_lens(ids, out=lens_np)
         mcl = int(lens_np.max())
-        pa.pa_decode_step_host(out_h[j], qh[j], kh[j], vh[j], slots_h[j], tables_h[j],
-                               lens_h[j], r.key_cache, r.value_cache, mcl, w.scale, staging,
-                               workspace=r.workspace, status=r.status, stream=stream)
-        done[j].record(stream)
+        pa.pa_decode_step_host_overlapped(out_h[j], qh[j], kh[j], vh[j], slots_h[j], tables_h[j],
+                                          lens_h[j], r.key_cache, r.value_cache, mcl, w.scale,
+                                          staging[j], stream, h2d_stream, d2h_stream, staged[j],
+                                          stepped[j], workspace=r.workspace, status=r.status)
+        done[j].record(d2h_stream)     # after the step's D2H
         pending[j] = int(lens_np.astype(np.int64).sum())
 
     for i in range(warm):
@@ -444,8 +451,9 @@ def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
             "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": 1e3 * dt / K,
             "seq_tokens_per_s": stats["tokens"] / dt,
             "path": "per step: pa_alloc_append_batch / block tables / lengths into pinned host "
-                    "buffers, pa_decode_step_host (H2D of q/k/v/metadata, reshape + decode, D2H "
-                    "of out); the host prepares step i+1 while the GPU runs step i and waits "
+                    "buffers, pa_decode_step_host_overlapped (H2D of q/k/v/metadata on an H2D "
+                    "stream, reshape + decode on the compute stream, D2H of out on a D2H "
+                    "stream); the host prepares step i+1 while the GPU runs step i and waits "
                     "for each step's output before reusing its buffers (ring of 3); wall clock"}
 
 

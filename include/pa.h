@@ -268,6 +268,27 @@ pa_status pa_decode_step_host(void* out_host, const void* query_host, const void
                               void* staging, size_t staging_bytes, void* workspace,
                               size_t workspace_bytes, int32_t* status_dev, pa_stream stream);
 
+/* pa_decode_step_host with the copies on streams of their own, so that a step's copies
+ * overlap the kernels of its neighbours.  On `h2d`: the H2D copies, then `staged_event` is
+ * recorded; on `compute`: wait for `staged_event`, pa_decode_step, record `done_event`; on
+ * `d2h`: wait for `done_event`, the D2H copy of out.  `h2d` and `d2h` must differ from
+ * `compute` (they may be one stream, but then a step's input copies queue behind the
+ * previous step's output copy, which waits for its kernels).  The events are cudaEvent_t
+ * owned by the caller.  A caller that keeps several steps in flight gives each its own
+ * staging area, host buffers and events, and reuses them only once that step's D2H has
+ * completed (for example an event it records on `d2h` after this call).  Steps must be
+ * issued in order: they share the KV pools and the workspace on `compute`.
+ * PA_ERR_INVALID_ARG when an event is NULL or a copy stream is `compute`. */
+pa_status pa_decode_step_host_overlapped(
+    void* out_host, const void* query_host, const void* key_host, const void* value_host,
+    const int32_t* slot_mapping_host, const int32_t* block_tables_host,
+    const int32_t* context_lens_host, void* key_cache, void* value_cache,
+    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_size, int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+    float scale, pa_dtype dtype, void* staging, size_t staging_bytes, void* workspace,
+    size_t workspace_bytes, int32_t* status_dev, pa_stream compute, pa_stream h2d,
+    pa_stream d2h, void* staged_event, void* done_event);
+
 /* Compute path for grouped-query attention (group >= 2): 1 (default) contracts the
  * group's query heads with each K/V tile on the tensor cores (mma.sync m16n8k16, fp32
  * accumulate); 0 uses the CUDA-core path that multi-head attention always takes.

@@ -85,6 +85,9 @@ def _load():
         "pa_decode_step_host_staging_size": ([i32, i32, i32, i32, i32], sz),
         "pa_decode_step_host": ([P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                  f32, i32, P, sz, P, sz, P, P], i32),
+        "pa_decode_step_host_overlapped": ([P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                            i32, i32, f32, i32, P, sz, P, sz, P, P, P, P, P, P],
+                                           i32),
         "pa_alloc_create": ([i32, i32, u64, ctypes.POINTER(P)], i32),
         "pa_alloc_destroy": ([P], None),
         "pa_alloc_num_free": ([P], i32),
@@ -417,6 +420,34 @@ def pa_decode_step_host(out_host, query_host, key_host, value_host, slot_mapping
         _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), maxb, S, Hq, Hkv, D, bs, NB,
         int(max_context_len), float(scale), dt, sp, sb, wp, wb, _opt_dev(status, "status"),
         _stream(stream)))
+
+
+def pa_decode_step_host_overlapped(out_host, query_host, key_host, value_host,
+                                   slot_mapping_host, block_tables_host, context_lens_host,
+                                   key_cache, value_cache, max_context_len: int, scale: float,
+                                   staging, compute_stream, h2d_stream, d2h_stream, staged_event,
+                                   done_event, workspace=None, status=None):
+    """pa_decode_step_host with the copies on `h2d_stream` / `d2h_stream` (see pa.h); the
+    events are torch.cuda.Event objects already recorded once (so that the CUDA events
+    exist)."""
+    S, Hq, D = query_host.shape
+    NB, Hkv, bs, D2 = key_cache.shape
+    if key_host.shape != (S, Hkv, D) or value_host.shape != key_host.shape or D2 != D:
+        raise ValueError("decode_step_host: key/value [S, Hkv, D] expected")
+    if out_host.shape != query_host.shape or tuple(slot_mapping_host.shape) != (S,):
+        raise ValueError("decode_step_host: out [S, Hq, D] and slot_mapping [S] expected")
+    maxb = int(block_tables_host.shape[1])
+    wp, wb = _ws(workspace)
+    sp, sb = _ws(staging)
+    _check(_lib.pa_decode_step_host_overlapped(
+        _host(out_host, "out_host"), _host(query_host, "query_host"), _host(key_host, "key_host"),
+        _host(value_host, "value_host"), _host(slot_mapping_host, "slot_mapping_host"),
+        _host(block_tables_host, "block_tables_host"), _host(context_lens_host, "context_lens_host"),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), maxb, S, Hq, Hkv, D, bs, NB,
+        int(max_context_len), float(scale), _dt(key_cache), sp, sb, wp, wb,
+        _opt_dev(status, "status"), _stream(compute_stream), _stream(h2d_stream),
+        _stream(d2h_stream), ctypes.c_void_p(staged_event.cuda_event),
+        ctypes.c_void_p(done_event.cuda_event)))
 
 
 def pa_set_kernel_events(start_event, stop_event):

@@ -481,15 +481,20 @@ size_t pa_decode_step_host_staging_size(int32_t num_seqs, int32_t num_q_heads, i
     return staging_layout(num_seqs, num_q_heads, num_kv_heads, head_size, max_blocks_per_seq).total;
 }
 
-pa_status pa_decode_step_host(void* out_host, const void* query_host, const void* key_host,
-                              const void* value_host, const int32_t* slot_mapping_host,
-                              const int32_t* block_tables_host, const int32_t* context_lens_host,
-                              void* key_cache, void* value_cache, int32_t max_blocks_per_seq,
-                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                              int32_t head_size, int32_t block_size, int32_t num_blocks,
-                              int32_t max_context_len, float scale, pa_dtype dtype, void* staging,
-                              size_t staging_bytes, void* workspace, size_t workspace_bytes,
-                              int32_t* status_dev, pa_stream stream) {
+namespace {
+
+// pa_decode_step_host and pa_decode_step_host_overlapped: the input copies go on `h2d`,
+// the step on `compute`, the output copy on `d2h`; with events the streams are ordered
+// through them (see pa.h), with one stream and no events everything is in stream order.
+pa_status step_host(void* out_host, const void* query_host, const void* key_host,
+                    const void* value_host, const int32_t* slot_mapping_host,
+                    const int32_t* block_tables_host, const int32_t* context_lens_host,
+                    void* key_cache, void* value_cache, int32_t max_blocks_per_seq,
+                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                    int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                    pa_dtype dtype, void* staging, size_t staging_bytes, void* workspace,
+                    size_t workspace_bytes, int32_t* status_dev, cudaStream_t compute,
+                    cudaStream_t h2d, cudaStream_t d2h, cudaEvent_t staged, cudaEvent_t done) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
         max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID_ARG, "decode_step_host: sizes must be positive");
@@ -505,8 +510,8 @@ pa_status pa_decode_step_host(void* out_host, const void* query_host, const void
     if (reinterpret_cast<uintptr_t>(staging) & 255u)
         return fail(PA_ERR_INVALID_ARG, "decode_step_host: staging must be 256-byte aligned");
     uint8_t* st = static_cast<uint8_t*>(staging);
-    cudaStream_t cs = (cudaStream_t)stream;
     const size_t S = (size_t)num_seqs;
+    cudaError_t e;
     struct Copy {
         void* dst;
         const void* src;
@@ -520,20 +525,71 @@ pa_status pa_decode_step_host(void* out_host, const void* query_host, const void
         {st + L.lens, context_lens_host, S * 4},
     };
     for (const Copy& c : copies) {
-        cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, cs);
+        e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, h2d);
         if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: H2D copy");
+    }
+    if (staged) {
+        if ((e = cudaEventRecord(staged, h2d)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(compute, staged, 0)) != cudaSuccess)
+            return cuda_fail(e, "decode_step_host: staged event");
     }
     pa_status ps = pa_decode_step(
         st + L.out, st + L.q, st + L.k, st + L.v, key_cache, value_cache,
         reinterpret_cast<const int32_t*>(st + L.slots), reinterpret_cast<const int32_t*>(st + L.tables),
         max_blocks_per_seq, reinterpret_cast<const int32_t*>(st + L.lens), num_seqs, num_q_heads,
         num_kv_heads, head_size, block_size, num_blocks, max_context_len, scale, dtype, workspace,
-        workspace_bytes, status_dev, stream);
+        workspace_bytes, status_dev, (pa_stream)compute);
     if (ps != PA_OK) return ps;
-    cudaError_t e = cudaMemcpyAsync(out_host, st + L.out, S * num_q_heads * head_size * 2,
-                                    cudaMemcpyDeviceToHost, cs);
+    if (done) {
+        if ((e = cudaEventRecord(done, compute)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(d2h, done, 0)) != cudaSuccess)
+            return cuda_fail(e, "decode_step_host: done event");
+    }
+    e = cudaMemcpyAsync(out_host, st + L.out, S * num_q_heads * head_size * 2,
+                        cudaMemcpyDeviceToHost, d2h);
     if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: D2H copy");
     return ok();
+}
+
+}  // namespace
+
+pa_status pa_decode_step_host(void* out_host, const void* query_host, const void* key_host,
+                              const void* value_host, const int32_t* slot_mapping_host,
+                              const int32_t* block_tables_host, const int32_t* context_lens_host,
+                              void* key_cache, void* value_cache, int32_t max_blocks_per_seq,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, int32_t block_size, int32_t num_blocks,
+                              int32_t max_context_len, float scale, pa_dtype dtype, void* staging,
+                              size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                              int32_t* status_dev, pa_stream stream) {
+    cudaStream_t cs = (cudaStream_t)stream;
+    return step_host(out_host, query_host, key_host, value_host, slot_mapping_host,
+                     block_tables_host, context_lens_host, key_cache, value_cache,
+                     max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_size,
+                     block_size, num_blocks, max_context_len, scale, dtype, staging, staging_bytes,
+                     workspace, workspace_bytes, status_dev, cs, cs, cs, nullptr, nullptr);
+}
+
+pa_status pa_decode_step_host_overlapped(
+    void* out_host, const void* query_host, const void* key_host, const void* value_host,
+    const int32_t* slot_mapping_host, const int32_t* block_tables_host,
+    const int32_t* context_lens_host, void* key_cache, void* value_cache,
+    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_size, int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+    float scale, pa_dtype dtype, void* staging, size_t staging_bytes, void* workspace,
+    size_t workspace_bytes, int32_t* status_dev, pa_stream compute, pa_stream h2d,
+    pa_stream d2h, void* staged_event, void* done_event) {
+    if (!staged_event || !done_event)
+        return fail(PA_ERR_INVALID_ARG, "decode_step_host_overlapped: both events are needed");
+    if (compute == h2d || compute == d2h)
+        return fail(PA_ERR_INVALID_ARG, "decode_step_host_overlapped: the copies need streams of their own");
+    return step_host(out_host, query_host, key_host, value_host, slot_mapping_host,
+                     block_tables_host, context_lens_host, key_cache, value_cache,
+                     max_blocks_per_seq, num_seqs, num_q_heads, num_kv_heads, head_size,
+                     block_size, num_blocks, max_context_len, scale, dtype, staging, staging_bytes,
+                     workspace, workspace_bytes, status_dev, (cudaStream_t)compute,
+                     (cudaStream_t)h2d, (cudaStream_t)d2h, static_cast<cudaEvent_t>(staged_event),
+                     static_cast<cudaEvent_t>(done_event));
 }
 
 pa_status pa_advance_step(int32_t* context_lens, int32_t* slot_mapping, const int32_t* block_tables,

@@ -48,6 +48,73 @@ def test_decode_step_host_matches_device_step_and_oracle(cuda_device):
                    w.dtype) <= TOL[w.dtype]
 
 
+def test_decode_step_host_overlapped_matches_device_steps(cuda_device):
+    """Four steps through pa_decode_step_host_overlapped (copies on their own streams, a ring
+    of two staging areas, each step queued before the previous one's output is read) give
+    the same bits as the same four steps taken from device buffers."""
+    import paged_kv_cache_187_gb300 as pa
+    from paged_kv_cache_187_gb300 import workloads as W
+    base = W.WORKLOADS["l3_8b"]
+    w = dataclasses.replace(base, num_seqs=32, steps=4)
+    lens = W.start_context_lens(base)[:32]
+    ra = _runner(w, start_lens=lens)
+    rb = _runner(w, start_lens=lens)
+    compute = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ring = 2
+    size = pa.pa_decode_step_host_staging_size(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                               w.head_size, rb.max_blocks)
+    staging = [torch.empty(size, dtype=torch.uint8, device=cuda_device) for _ in range(ring)]
+    staged = [torch.cuda.Event() for _ in range(ring)]
+    done = [torch.cuda.Event() for _ in range(ring)]
+    fin = [torch.cuda.Event() for _ in range(ring)]
+    for e in staged + done + fin:
+        e.record(d2h)
+    pin = lambda t: t.cpu().pin_memory()
+    pending = [None] * ring
+    checked = 0
+
+    def check(j):
+        nonlocal checked
+        if pending[j] is None:
+            return
+        out_h, ref = pending[j]
+        fin[j].synchronize()
+        assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16))
+        pending[j] = None
+        checked += 1
+
+    for i in range(4):
+        ra.next_step()
+        ra.run_step()
+        ref = ra.out.cpu()
+        rb.next_step()
+        j = i % ring
+        check(j)          # the slot's previous step has been read back
+        out_h = torch.empty(rb.out.shape, dtype=rb.out.dtype).pin_memory()
+        pa.pa_decode_step_host_overlapped(
+            out_h, pin(rb.q), pin(rb.k_new), pin(rb.v_new),
+            torch.from_numpy(rb.slots).pin_memory(), torch.from_numpy(rb.block_tables).pin_memory(),
+            torch.from_numpy(rb.context_lens).pin_memory(), rb.key_cache, rb.value_cache,
+            rb.step_max_context_len(), w.scale, staging[j], compute, h2d, d2h, staged[j], done[j],
+            workspace=rb.workspace, status=rb.status)
+        fin[j].record(d2h)
+        pending[j] = (out_h, ref)
+    for j in range(ring):
+        check(j)
+    assert checked == 4
+    torch.cuda.synchronize()
+    assert int(rb.status.item()) == 0
+    assert torch.equal(rb.key_cache.view(torch.int16), ra.key_cache.view(torch.int16))
+    with pytest.raises(pa.PAError):   # the copies on the compute stream
+        pa.pa_decode_step_host_overlapped(
+            out_h, pin(rb.q), pin(rb.k_new), pin(rb.v_new),
+            torch.from_numpy(rb.slots).pin_memory(), torch.from_numpy(rb.block_tables).pin_memory(),
+            torch.from_numpy(rb.context_lens).pin_memory(), rb.key_cache, rb.value_cache,
+            rb.step_max_context_len(), w.scale, staging[0], compute, compute, d2h, staged[0], done[0],
+            workspace=rb.workspace, status=rb.status)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(cuda_device):
     import paged_kv_cache_187_gb300 as pa
     from paged_kv_cache_187_gb300 import workloads as W
