@@ -190,13 +190,15 @@ struct DecodeArgs {
 
 // The tcgen05 multi-query kernel takes head_size 128, 16-bit caches, and partitions that
 // are multiples of its 128-token tile; it holds 16 or 32 query rows per unit.  It is used
-// from 9 query rows per kv head on: with fewer rows the mma.sync kernel's three CTAs per
-// SM hide the load latency better than its single tile pipeline per SM (measured on the
-// Llama-3-8B / -70B batches: 8 rows 231 vs 197 us; 16 rows 246 vs 266 us and 685 vs
-// 647 us; 32 rows 365 vs 366 us and 924 vs 1034 us).
+// where it measured faster than the mma.sync kernel, whose three CTAs per SM hide the load
+// latency better than its single tile pipeline per SM: above 16 query rows per kv head,
+// and above 8 with 16-token blocks (Llama-3-8B / -70B batches: 8 rows 231 vs 197 us;
+// 16 rows 244 vs 266 us with 16-token blocks, 690 vs 647 us with 32-token blocks; 32 rows
+// 357 vs 366 us and 928 vs 1034 us).
 bool use_mq_tc(const DecodeArgs& a) {
     const int32_t rows = a.q_len * (a.num_q_heads / std::max(a.num_kv_heads, 1));
-    return g_mq_tc && a.q_len > 1 && rows > 8 && a.head_size == 128 && !a.kv8 &&
+    const bool wins = rows > 16 || (rows > 8 && a.block_size == 16);
+    return g_mq_tc && a.q_len > 1 && wins && a.head_size == 128 && !a.kv8 &&
            (a.partition_size == 0 || a.partition_size % pa::kTcTileTokens == 0);
 }
 int32_t mq_tc_rows(int32_t rows) { return rows <= 16 ? 16 : 32; }

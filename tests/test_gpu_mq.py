@@ -58,9 +58,9 @@ def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
 
 
 # (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group.  With
-# head_size 128 and more than 8 rows the tcgen05 kernel takes the case (16 or 32 rows per
-# unit) unless the test switches it off; otherwise the mma.sync kernel (up to 4 row groups
-# of 8 rows per unit).
+# head_size 128 the tcgen05 kernel takes cases above 16 rows, or above 8 with 16-token
+# blocks (16 or 32 rows per unit), unless the test switches it off; otherwise the mma.sync
+# kernel (up to 4 row groups of 8 rows per unit).
 CASES = [
     ("bf16", 4, 32, 8, 128, 16),   # 16 rows: one 16-row unit (Llama-3-8B heads)
     ("f16", 2, 32, 8, 128, 32),    # 8 rows, 32-token blocks
@@ -72,6 +72,7 @@ CASES = [
     ("f16", 8, 8, 1, 64, 32),      # 64 rows: two units of two full row groups
     ("f16", 4, 16, 2, 128, 32),    # 32 rows, 32-token blocks
     ("bf16", 3, 32, 8, 128, 32),   # 12 rows, 32-token blocks
+    ("bf16", 3, 32, 8, 128, 16),   # 12 rows, 16-token blocks
 ]
 
 
