@@ -281,7 +281,9 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(device)
     variant, psize = pa.pa_decode_auto_plan(w.num_seqs, w.num_q_heads, w.num_kv_heads,
                                             w.head_size, w.block_size, r.step_max_context_len())
-    launches_per_step = 1 + (1 if variant == 1 else 2 + (1 if r.step_max_context_len() > psize else 0))
+    # reshape_and_cache, then the decode (V1) or the plan and the decode (V2: the
+    # partition merge runs inside the decode kernel)
+    launches_per_step = 2 if variant == 1 else 3
     bytes_step = r.kv_bytes()
     tokens_step = r.seq_tokens()
 
