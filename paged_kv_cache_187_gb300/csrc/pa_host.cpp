@@ -201,7 +201,10 @@ bool use_mq_tc(const DecodeArgs& a) {
     return g_mq_tc && a.q_len > 1 && wins && a.head_size == 128 && !a.kv8 &&
            (a.partition_size == 0 || a.partition_size % pa::kTcTileTokens == 0);
 }
-int32_t mq_tc_rows(int32_t rows) { return rows <= 16 ? 16 : 32; }
+// Rows per unit of the tcgen05 kernel (16-row units exist for 16-token blocks only).
+int32_t mq_tc_rows(int32_t rows, int32_t block_size) {
+    return rows <= 16 && block_size == 16 ? 16 : 32;
+}
 
 // Multi-query kernels: rows per consumer (the head capacity), consumer warps per CTA, row
 // groups per unit (a power of two dividing the consumers, so that the consumers of a
@@ -267,7 +270,7 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
         k.mma = true;
         if (use_mq_tc(a)) {
             k.tc = true;
-            k.heads_cap = mq_tc_rows(a.q_len * g);
+            k.heads_cap = mq_tc_rows(a.q_len * g, a.block_size);
             return k;
         }
         k.heads_cap = mq_heads_cap(a.q_len * g);
@@ -301,7 +304,7 @@ pa::DecodeParams base_params(const DecodeArgs& a) {
     p.q_len = a.q_len;
     p.rows = a.q_len * p.group;
     if (use_mq_tc(a)) {
-        const int32_t r = mq_tc_rows(p.rows);
+        const int32_t r = mq_tc_rows(p.rows, a.block_size);
         p.row_chunks = (p.rows + r - 1) / r;
         p.row_groups = 1;
         p.partition_align = pa::kTcTileTokens;

@@ -73,6 +73,7 @@ CASES = [
     ("f16", 4, 16, 2, 128, 32),    # 32 rows, 32-token blocks
     ("bf16", 3, 32, 8, 128, 32),   # 12 rows, 32-token blocks
     ("bf16", 3, 32, 8, 128, 16),   # 12 rows, 16-token blocks
+    ("f16", 2, 64, 8, 128, 16),    # 16 rows, fp16 (one P term on tcgen05)
 ]
 
 
