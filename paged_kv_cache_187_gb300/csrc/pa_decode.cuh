@@ -117,10 +117,14 @@ struct UnitDesc {
 };
 
 template <int D_, int BS_, bool BF16_, bool MMA_, int HCAP_, int NSTAGE_, int NQ_, int NCONS_,
-          bool KV8_ = false, bool MQ_ = false, int MINB_ = 0>
+          bool KV8_ = false, bool MQ_ = false, int MINB_ = 0, int PBS_ = BS_>
 struct DecodeCfg {
     static constexpr int D = D_;
+    // Tokens per tile (what a consumer takes at a time), and the pool's block size: a tile
+    // is TB = BS / PBS consecutive blocks of the sequence, gathered into one stage.
     static constexpr int BS = BS_;
+    static constexpr int PBS = PBS_;
+    static constexpr int TB = BS_ / PBS_;
     static constexpr bool kBf16 = BF16_;           // query / output type (bf16 or fp16)
     static constexpr bool kKv8 = KV8_;             // K/V cache in fp8 E4M3 (else = query type)
     static constexpr bool kMma = MMA_;
@@ -132,7 +136,7 @@ struct DecodeCfg {
     static constexpr int NCONS = NCONS_;           // consumer warps per CTA
     static constexpr int ELEM = KV8_ ? 1 : 2;      // bytes per cached element
     static constexpr int HALVES = D * ELEM / 128;  // 128-byte swizzle spans per row
-    static constexpr int TILE_BYTES = D * BS * ELEM;  // one (block, kv head) tile of K or V
+    static constexpr int TILE_BYTES = D * BS * ELEM;  // one tile of K or V (one kv head)
     static constexpr int HALF_BYTES = BS * 128;
     // multi-query: a unit has up to NCONS row groups of HCAP rows, each finished by its
     // own consumer
@@ -144,7 +148,8 @@ struct DecodeCfg {
     // per-lane floats of one consumer's softmax state (m, l, acc)
     static constexpr int NSTATE = MMA_ ? (4 * NT + (D / 16) * NT * 4) : (2 * HCAP_ + HCAP_ * (D / 32));
     static_assert(D == 64 || D == 128, "head_size");
-    static_assert(BS == 16 || BS == 32, "block_size");
+    static_assert(BS == 16 || BS == 32, "tile tokens");
+    static_assert((PBS_ == 16 || PBS_ == 32) && BS_ % PBS_ == 0, "block_size");
     static_assert(!MMA_ || HCAP_ == 8 || HCAP_ == 16, "mma heads");
     static_assert(MMA_ || HCAP_ == 1 || HCAP_ == 2 || HCAP_ == 4 || HCAP_ == 8, "heads");
     static_assert(NCONS >= 1 && NCONS <= 4, "consumers");
@@ -1035,7 +1040,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
         // Loads (all lanes, one entry each) block-table entries b0 .. b0+31 of a unit,
         // replacing entries outside the pool by a row past the tensor map (TMA reads zeros).
         auto load_blocks = [&](const UnitDesc& u, int32_t b0, int32_t n) {
-            int32_t phys = 0;
+            int32_t phys = p.num_blocks;   // past the unit: a row past the tensor map (zeros)
             if (lane < n) {
                 phys = p.block_tables[(size_t)u.seq * p.max_blocks_per_seq + b0 + lane];
                 if (phys < 0 || phys >= p.num_blocks) {
@@ -1116,30 +1121,40 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 } else if (step == 2) {
                     if (w_next < total) {
                         const UnitDesc un = describe(w_next, e_next, false);
-                        const int32_t nb0 = un.tok0 / C::BS, nb1 = (un.tok1 + C::BS - 1) / C::BS;
+                        const int32_t nb0 = un.tok0 / C::PBS, nb1 = (un.tok1 + C::PBS - 1) / C::PBS;
                         next_phys = load_blocks(un, nb0, min(32, nb1 - nb0));
                     }
                     step = 3;
                 }
             };
-            const int32_t b0 = u.tok0 / C::BS, b1 = (u.tok1 + C::BS - 1) / C::BS;
-            if (b1 - b0 <= kClaimLead) advance_next();
-            for (int32_t jb = b0; jb < b1 && ok; jb += 32) {
-                const int32_t n = min(32, b1 - jb);
-                const int32_t phys = (jb == b0 && have_pre) ? pre_phys : load_blocks(u, jb, n);
-                for (int32_t i = 0; i < n; ++i) {
-                    const int32_t pb = __shfl_sync(0xffffffffu, phys, i);
+            // The unit's paged blocks nb0 .. nb1-1, TB per tile (the last tile's blocks past
+            // nb1 read as zeros), block-table entries 32 at a time.
+            const int32_t nb0 = u.tok0 / C::PBS, nb1 = (u.tok1 + C::PBS - 1) / C::PBS;
+            const int32_t ntiles = (u.tok1 - u.tok0 + C::BS - 1) / C::BS;
+            if (ntiles <= kClaimLead) advance_next();
+            for (int32_t jb = nb0; jb < nb0 + ntiles * C::TB && ok; jb += 32) {
+                const int32_t n = min(32, nb1 - jb);
+                const int32_t phys = (jb == nb0 && have_pre) ? pre_phys : load_blocks(u, jb, n);
+                const int32_t tile_base = (jb - nb0) / C::TB;   // first tile of this chunk
+                for (int32_t i = 0; i < 32 / C::TB && tile_base + i < ntiles; ++i) {
+                    int32_t pb[C::TB];
+#pragma unroll
+                    for (int bi = 0; bi < C::TB; ++bi) pb[bi] = __shfl_sync(0xffffffffu, phys, i * C::TB + bi);
                     if (lane == 0) {
                         ok = mbar_wait(&sm.empty[stage], ephase);
                         if (ok) {
                             mbar_arrive_expect_tx(&sm.full[stage], 2u * C::TILE_BYTES);
-                            const int32_t y = (pb * Hkv + u.kvh) * C::BS;
 #pragma unroll
-                            for (int h = 0; h < C::HALVES; ++h) {
-                                tma_load_2d(sm.kv[stage][0] + h * C::HALF_BYTES, &kmap, h * 64, y,
-                                            &sm.full[stage], policy);
-                                tma_load_2d(sm.kv[stage][1] + h * C::HALF_BYTES, &vmap, h * 64, y,
-                                            &sm.full[stage], policy);
+                            for (int bi = 0; bi < C::TB; ++bi) {
+                                const int32_t y = (pb[bi] * Hkv + u.kvh) * C::PBS;
+                                const uint32_t off = bi * C::PBS * 128;
+#pragma unroll
+                                for (int h = 0; h < C::HALVES; ++h) {
+                                    tma_load_2d(sm.kv[stage][0] + h * C::HALF_BYTES + off, &kmap, h * 64, y,
+                                                &sm.full[stage], policy);
+                                    tma_load_2d(sm.kv[stage][1] + h * C::HALF_BYTES + off, &vmap, h * 64, y,
+                                                &sm.full[stage], policy);
+                                }
                             }
                             sm.issued[stage] += 1;
                         }
@@ -1150,7 +1165,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                         stage = 0;
                         ephase ^= 1;
                     }
-                    if (step > 0 || b1 - (jb + i + 1) <= kClaimLead) advance_next();
+                    if (step > 0 || ntiles - (tile_base + i + 1) <= kClaimLead) advance_next();
                 }
             }
             if (!ok) {

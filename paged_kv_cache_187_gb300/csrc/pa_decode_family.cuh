@@ -78,15 +78,18 @@ constexpr int consumers_for() {
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
 }
 
-template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false, int MQC = 0>
+// BS: the pool's block size; TB: blocks per tile (a consumer step takes BS * TB tokens).
+template <int D, int BS, bool BF16, bool MMA, int HCAP, bool KV8 = false, int MQC = 0, int TB = 1>
 cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                        bool persistent, int32_t num_units, cudaStream_t stream,
                        int32_t* ctas_per_sm_out) {
     constexpr bool MQ = MQC > 0;
-    constexpr int kCons = consumers_for<MMA, BS, KV8, MQC>();
-    constexpr int kStages = stages_for<D * (KV8 ? 1 : 2) / 2, BS, kCons>();
-    using C = DecodeCfg<D, BS, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ,
-                        decode_min_ctas<DecodeCfg<D, BS, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ>>()>;
+    constexpr int kTile = BS * TB;
+    constexpr int kCons = consumers_for<MMA, kTile, KV8, MQC>();
+    constexpr int kStages = stages_for<D * (KV8 ? 1 : 2) / 2, kTile, kCons>();
+    using C0 = DecodeCfg<D, kTile, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ, 0, BS>;
+    using C = DecodeCfg<D, kTile, BF16, MMA, HCAP, kStages, 2, kCons, KV8, MQ,
+                        decode_min_ctas<C0>(), BS>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
     static bool configured = false;   // per instantiation; attribute setting is idempotent
@@ -122,6 +125,24 @@ template <int D, bool BF16, bool KV8 = false>
 cudaError_t launch_family(const KernelKey& k, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const DecodeParams& p, bool persistent, int32_t num_units,
                           cudaStream_t stream, int32_t* occ) {
+    // fp8 caches with 16-token blocks take two blocks per tile: a consumer step then has
+    // 32 tokens to amortise its softmax over, as with 32-token blocks
+    if constexpr (KV8) {
+        if (k.tile_blocks == 2) {
+#define PA_CASE2(MMA_, H_)                                                                   \
+    if (k.block_size == 16 && k.mma == MMA_ && k.heads_cap == H_)                            \
+        return launch_one<D, 16, BF16, MMA_, H_, KV8, 0, 2>(kmap, vmap, p, persistent,       \
+                                                           num_units, stream, occ);
+            PA_CASE2(true, 8)
+            PA_CASE2(true, 16)
+            PA_CASE2(false, 1)
+            PA_CASE2(false, 2)
+            PA_CASE2(false, 4)
+            PA_CASE2(false, 8)
+#undef PA_CASE2
+            return cudaErrorInvalidValue;
+        }
+    }
 #define PA_CASE(BS_, MMA_, H_)                                                            \
     if (k.block_size == BS_ && k.mma == MMA_ && k.heads_cap == H_)                        \
         return launch_one<D, BS_, BF16, MMA_, H_, KV8>(kmap, vmap, p, persistent, num_units, \

@@ -105,7 +105,8 @@ cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CU
 }
 
 int32_t ctas_per_sm(int dev, const pa::KernelKey& k) {
-    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.tc << 28 | (uint64_t)k.mq_consumers << 24 |
+    const uint64_t key = (uint64_t)dev << 32 | (uint64_t)k.tile_blocks << 29 | (uint64_t)k.tc << 28 |
+                         (uint64_t)k.mq_consumers << 24 |
                          (uint64_t)k.mq << 22 |
                          (uint64_t)k.kv8 << 21 |
                          (uint64_t)(k.head_size == 128) << 20 |
@@ -202,6 +203,13 @@ bool use_mq_tc(const DecodeArgs& a) {
            (a.partition_size == 0 || a.partition_size % pa::kTcTileTokens == 0);
 }
 // Rows per unit of the tcgen05 kernel (16-row units exist for 16-token blocks only).
+// fp8 caches with 16-token blocks are decoded in tiles of two blocks (32 tokens), which
+// needs partitions that are multiples of 32 tokens.
+int32_t tile_blocks_for(const DecodeArgs& a) {
+    return (a.kv8 && a.block_size == 16 && a.q_len == 1 &&
+            (a.partition_size == 0 || a.partition_size % 32 == 0)) ? 2 : 1;
+}
+
 int32_t mq_tc_rows(int32_t rows, int32_t block_size) {
     return rows <= 16 && block_size == 16 ? 16 : 32;
 }
@@ -280,6 +288,7 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
     k.mma = g >= 2 && (g > 8 || g_gqa_mma);
     if (k.mma) k.heads_cap = g <= 8 ? 8 : 16;
     else k.heads_cap = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
+    k.tile_blocks = tile_blocks_for(a);
     return k;
 }
 
@@ -311,6 +320,7 @@ pa::DecodeParams base_params(const DecodeArgs& a) {
     } else {
         p.row_chunks = a.q_len > 1 ? mq_row_chunks(p.rows) : 1;
         p.row_groups = a.q_len > 1 ? mq_row_groups(p.rows) : 1;
+        p.partition_align = a.block_size * tile_blocks_for(a);
     }
     return p;
 }

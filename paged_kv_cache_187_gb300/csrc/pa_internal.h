@@ -82,6 +82,7 @@ struct KernelKey {
     bool mq = false;     // several causal query tokens per sequence (tensor-core path only)
     int32_t mq_consumers = 0;   // multi-query: consumer warps per CTA (2 or 4)
     bool tc = false;            // multi-query on tcgen05 (heads_cap = rows per unit, 16 or 32)
+    int32_t tile_blocks = 1;    // pool blocks per consumer tile (2: fp8 with 16-token blocks)
 };
 
 // Launchers return cudaSuccess or the launch error.  `persistent` selects the V2

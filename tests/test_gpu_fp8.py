@@ -72,10 +72,11 @@ def test_fp8_cache_scatter_bit_exact_and_decode(cuda_device, dtype, Hq, Hkv, bs)
     lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
     mcl = int(b["lens"].max())
     ws = torch.empty(max(pa.pa_decode_auto_workspace_size(S, Hq, Hkv, 128, bs, mcl),
-                         pa.pa_decode_v2_workspace_size(S, Hq, 128, mcl, 4 * bs), 256),
+                         pa.pa_decode_v2_workspace_size(S, Hq, 128, mcl, 3 * bs), 256),
                      dtype=torch.uint8, device=cuda_device)
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    for variant, P in (("auto", 0), ("v1", 0), ("v2", 4 * bs)):
+    # with 16-token blocks, partitions of 4 blocks take the two-block tiles; of 3, one-block
+    for variant, P in (("auto", 0), ("v1", 0), ("v2", 4 * bs), ("v2", 3 * bs)):
         out.fill_(5.0)
         pa.pa_decode_fp8(out, b["q"], b["kc"], b["vc"], tables, lens_d, mcl, scale, b["ks"],
                          b["vs"], variant=variant, partition_size=P, workspace=ws, status=status)
