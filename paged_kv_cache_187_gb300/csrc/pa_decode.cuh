@@ -337,10 +337,20 @@ struct MmaConsumer {
     static __device__ __forceinline__ int k_dim_fp8(int i, int q, int j) {
         return 32 * q + 16 * (i >> 2) + 4 * (i & 3) + j;
     }
+    // fp8 tiles: the token of S^T row x (0..15) of a 16-token group.  The K rows are read
+    // in this order so that the P fragments pair tokens (4q, 4q+1) and (4q+2, 4q+3): the
+    // order in which the transposing 8-bit ldmatrix hands out the V^T fragments.
+    static __device__ __forceinline__ int fp8_row_token(int x) {
+        return 4 * ((x & 7) >> 1) + (x & 1) + 2 * (x >> 3);
+    }
+    // Token (within the tile) of S^T row lane/4 + 8 * (r / 2) of m-tile mt.
+    static __device__ __forceinline__ int score_token(int mt, int lane, int r) {
+        const int x = (lane >> 2) + 8 * (r >> 1);
+        return mt * 16 + (C::kKv8 ? fp8_row_token(x) : x);
+    }
     // Output head dim of accumulator (m-tile i, lane, register r).
     static __device__ __forceinline__ int out_dim(int i, int lane, int r) {
-        if constexpr (C::kKv8) return 32 * (i >> 1) + 4 * (lane >> 2) + 2 * (i & 1) + (r >> 1);
-        else return i * 16 + (lane >> 2) + 8 * (r >> 1);
+        return i * 16 + (lane >> 2) + 8 * (r >> 1);
     }
 
     __device__ __forceinline__ void load_q(const uint8_t* qbuf, int nrows, int lane) {
@@ -416,7 +426,7 @@ struct MmaConsumer {
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const int tk = mt * 16 + (lane >> 2) + 8 * (r >> 1);
+                    const int tk = score_token(mt, lane, r);
                     float v = sc[mt][nt][r] * scale_log2;
                     bool keep;
                     if constexpr (C::kMq) keep = tile0 + tk < lim[nt][r & 1];
@@ -475,12 +485,12 @@ struct MmaConsumer {
     }
 
     // fp8 E4M3 tile [BS][128 B] (swizzled).  K: lane (g = lane/4, q = lane%4) reads 16
-    // contiguous bytes (k-steps 4h..4h+3 in the permuted head-dim order) of rows g and
-    // g+8 per 16-token group -- conflict-free, since the 128B swizzle puts the even and
-    // odd chunks of neighbouring rows in different banks.  V^T: for m-tile pair pp the
-    // lane reads 4 bytes (dims 32pp + 4g .. +3) of each of its tokens 2q, 2q+1, 2q+8,
-    // 2q+9 and assembles the fragments with byte permutes; the output dims come out in
-    // the matching order (out_dim).
+    // contiguous bytes (k-steps 4h..4h+3 in the permuted head-dim order) of S^T rows g
+    // and g+8 of each 16-token group, i.e. of tokens fp8_row_token(g), fp8_row_token(g+8)
+    // -- an even and an odd token, whose chunks the 128B swizzle puts in different banks.
+    // V^T: the transposing 8-bit ldmatrix gives the lane head dims g and g+8 of tokens
+    // 4q .. 4q+3, which widen to fp16 fragments as they stand (k-slots 2q, 2q+1 = tokens
+    // 4q, 4q+1; k-slots 2q+8, 2q+9 = tokens 4q+2, 4q+3, matching the P fragments).
     __device__ __forceinline__ void tile_fp8(const uint8_t* kt, const uint8_t* vt, int valid,
                                              float scale_log2, int lane) {
         const int g = lane >> 2, q = lane & 3;
@@ -493,7 +503,7 @@ struct MmaConsumer {
                 for (int r = 0; r < 4; ++r) sc[mt][nt][r] = sc2[mt][nt][r] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const int t0 = mt * 16 + g, t1 = t0 + 8;
+            const int t0 = mt * 16 + fp8_row_token(g), t1 = mt * 16 + fp8_row_token(g + 8);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint4 w0 = *reinterpret_cast<const uint4*>(kt + swz<C>(t0, 2 * q + h));
@@ -523,30 +533,35 @@ struct MmaConsumer {
         uint32_t pb[MT][NT][2], pl[MT][NT][2];
         softmax_tile(sc, valid, 0, scale_log2, lane, pb, pl);
         const bool ragged = valid < BS;
+        const uint32_t vbase = smem_u32(vt);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const int tq = mt * 16 + 2 * q;
-            uint32_t keep0 = 0xffffffffu, keep8 = 0xffffffffu;
+            // this lane's V^T fragments hold tokens 4q .. 4q+3 of the 16-token group
+            uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
             if (ragged) {
-                keep0 = ((tq < valid) ? 0x0000ffffu : 0u) | ((tq + 1 < valid) ? 0xffff0000u : 0u);
-                keep8 = ((tq + 8 < valid) ? 0x0000ffffu : 0u) | ((tq + 9 < valid) ? 0xffff0000u : 0u);
+                // Rows past the context may hold anything (NaN included): zero them so
+                // that 0 * NaN never reaches the accumulator.
+                const int tq = mt * 16 + 4 * q;
+                keep_lo = ((tq < valid) ? 0x0000ffffu : 0u) | ((tq + 1 < valid) ? 0xffff0000u : 0u);
+                keep_hi = ((tq + 2 < valid) ? 0x0000ffffu : 0u) | ((tq + 3 < valid) ? 0xffff0000u : 0u);
             }
 #pragma unroll
-            for (int pp = 0; pp < D / 32; ++pp) {
-                const int byte = 32 * pp + 4 * g;
-                const uint32_t v0 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq, byte >> 4) + (byte & 15));
-                const uint32_t v1 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq + 1, byte >> 4) + (byte & 15));
-                const uint32_t v8 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq + 8, byte >> 4) + (byte & 15));
-                const uint32_t v9 = *reinterpret_cast<const uint32_t*>(vt + swz<C>(tq + 9, byte >> 4) + (byte & 15));
+            for (int c2 = 0; c2 < D / 32; ++c2) {
+                // head dims 32 c2 .. 32 c2 + 31: two 16x16 byte blocks (tokens x dims)
+                uint32_t r[4];
+                ldmatrix_b8_trans_x2(r, vbase + swz<C>(mt * 16 + (lane & 15), 2 * c2 + (lane >> 4)));
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
+                for (int h = 0; h < 2; ++h) {
                     uint32_t a[4];
-                    // byte 2e+f of each token's word is head dim 32pp + 4g + 2e + f
-                    a[0] = e4m3x2_to_f16x2(__byte_perm(v0, v1, (2 * e) | ((4 + 2 * e) << 4))) & keep0;
-                    a[1] = e4m3x2_to_f16x2(__byte_perm(v0, v1, (2 * e + 1) | ((5 + 2 * e) << 4))) & keep0;
-                    a[2] = e4m3x2_to_f16x2(__byte_perm(v8, v9, (2 * e) | ((4 + 2 * e) << 4))) & keep8;
-                    a[3] = e4m3x2_to_f16x2(__byte_perm(v8, v9, (2 * e + 1) | ((5 + 2 * e) << 4))) & keep8;
-                    const int i = 2 * pp + e;
+                    e4m3x4_to_f16x2x2(r[2 * h], a[0], a[2]);       // dim g:   tokens 4q..4q+3
+                    e4m3x4_to_f16x2x2(r[2 * h + 1], a[1], a[3]);   // dim g+8
+                    if (ragged) {
+                        a[0] &= keep_lo;
+                        a[1] &= keep_lo;
+                        a[2] &= keep_hi;
+                        a[3] &= keep_hi;
+                    }
+                    const int i = 2 * c2 + h;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         mma_16816<false>(acc[i][nt], a, pb[mt][nt][0], pb[mt][nt][1]);

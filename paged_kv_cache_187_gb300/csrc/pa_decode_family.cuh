@@ -50,6 +50,11 @@ constexpr int stages_for() {
 //     heads the same bound would cost those kernels a CTA.)
 //   * 4-consumer multi-query kernels (5 warps): sized for the 2 CTAs their shared memory
 //     admits (168 registers instead of the compiler's 128 with spills).
+// Two-block tiles for 16-bit caches with 16-token blocks too (off: measured slower).
+#ifndef PA_TILE2_16BIT
+#define PA_TILE2_16BIT 0
+#endif
+
 #ifndef PA_CORE_MIN_CTAS
 #define PA_CORE_MIN_CTAS 1
 #endif
@@ -127,7 +132,7 @@ cudaError_t launch_family(const KernelKey& k, const CUtensorMap& kmap, const CUt
                           cudaStream_t stream, int32_t* occ) {
     // fp8 caches with 16-token blocks take two blocks per tile: a consumer step then has
     // 32 tokens to amortise its softmax over, as with 32-token blocks
-    if constexpr (KV8) {
+    if constexpr (KV8 || PA_TILE2_16BIT) {
         if (k.tile_blocks == 2) {
 #define PA_CASE2(MMA_, H_)                                                                   \
     if (k.block_size == 16 && k.mma == MMA_ && k.heads_cap == H_)                            \

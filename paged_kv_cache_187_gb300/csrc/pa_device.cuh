@@ -136,6 +136,16 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                  : "r"(addr));
 }
 
+// Two 16x16 matrices of 8-bit elements, transposed: lanes 0-15 give the addresses of
+// the 16 rows (16 bytes each) of matrix 0, lanes 16-31 those of matrix 1.  Lane (g =
+// lane/4, q = lane%4) receives for matrix k: r[2k] = column g, r[2k+1] = column g+8,
+// each as rows 4q .. 4q+3 (row 4q in the low byte).
+__device__ __forceinline__ void ldmatrix_b8_trans_x2(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));

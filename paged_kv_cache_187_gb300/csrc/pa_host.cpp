@@ -206,7 +206,10 @@ bool use_mq_tc(const DecodeArgs& a) {
 // fp8 caches with 16-token blocks are decoded in tiles of two blocks (32 tokens), which
 // needs partitions that are multiples of 32 tokens.
 int32_t tile_blocks_for(const DecodeArgs& a) {
-    return (a.kv8 && a.block_size == 16 && a.q_len == 1 &&
+#ifndef PA_TILE2_16BIT
+#define PA_TILE2_16BIT 0
+#endif
+    return ((a.kv8 || PA_TILE2_16BIT) && a.block_size == 16 && a.q_len == 1 &&
             (a.partition_size == 0 || a.partition_size % 32 == 0)) ? 2 : 1;
 }
 
