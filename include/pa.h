@@ -289,10 +289,11 @@ pa_status pa_decode_step_host_overlapped(
     size_t workspace_bytes, int32_t* status_dev, pa_stream compute, pa_stream h2d,
     pa_stream d2h, void* staged_event, void* done_event);
 
-/* Compute path for grouped-query attention (group >= 2): 1 (default) contracts the
- * group's query heads with each K/V tile on the tensor cores (mma.sync m16n8k16, fp32
- * accumulate); 0 uses the CUDA-core path that multi-head attention always takes.
- * Process-wide; both paths meet the same tolerance. */
+/* Compute path for grouped-query attention (group >= 2) and for fp8 caches of any
+ * group: 1 (default) contracts the group's query heads with each K/V tile on the tensor
+ * cores (mma.sync m16n8k16, fp32 accumulate); 0 uses the CUDA-core path that
+ * multi-head attention over 16-bit caches always takes.  Groups above 8 stay on the
+ * tensor cores.  Process-wide; both paths meet the same tolerance. */
 pa_status pa_set_gqa_tensor_cores(int32_t enable);
 
 /* ------------------------------------------------------------------------------ */

@@ -153,10 +153,11 @@ struct DecodeCfg {
     static_assert(!MMA_ || HCAP_ == 8 || HCAP_ == 16, "mma heads");
     static_assert(MMA_ || HCAP_ == 1 || HCAP_ == 2 || HCAP_ == 4 || HCAP_ == 8, "heads");
     static_assert(NCONS >= 1 && NCONS <= 4, "consumers");
-    // Consumer c takes tiles c, c + NCONS, ... of a unit, and tile k lands in stage
-    // k % NSTAGE.  With NSTAGE a multiple of NCONS, the previous use of a stage (tile
-    // k - NSTAGE) belongs to the same consumer, so a consumer never waits on a stage that
-    // is two phases behind -- where the mbarrier parity test would pass too early.
+    // Tile k (counted over all units) goes to consumer k % NCONS (of its row group) and
+    // lands in stage k % NSTAGE.  With NSTAGE a multiple of NCONS, the previous use of a
+    // stage (tile k - NSTAGE) belongs to the same consumer, so a consumer never waits on
+    // a stage that is two phases behind -- where the mbarrier parity test would pass too
+    // early.
     static_assert(NSTAGE % NCONS == 0, "stages must be a multiple of the consumer warps");
     static_assert(!KV8_ || D == 128, "fp8 K/V: head_size 128");
     static_assert(!MQ_ || (MMA_ && !KV8_), "multi-query: tensor-core path, 16-bit cache");
@@ -166,11 +167,11 @@ template <class C>
 struct alignas(1024) DecodeSmem {
     uint8_t kv[C::NSTAGE][2][C::TILE_BYTES];         // stage: K tile then V tile
     alignas(128) uint8_t qbuf[C::NQ][C::QROWS * C::D * 2];
-    // Output staging of consumer 0.  Multi-query kernels stage each row group's output
-    // in its leader's own xbuf slot instead (see the consumer loop).
+    // Output staging of a unit's leader.  Multi-query kernels stage each row group's
+    // output in one of the group's state slots instead (see the consumer loop).
     alignas(128) float ostage[C::kMq ? 1 : C::HCAP * C::D];
-    // Consumer c > 0 exports its softmax state to slot c - 1 for merging; multi-query
-    // kernels have one slot per consumer.
+    // State slots: the consumers other than a unit's leader export their softmax states
+    // here for merging (NCONS - 1 slots); multi-query kernels have one slot per consumer.
     alignas(16) float xbuf[C::kMq ? C::NCONS : (C::NCONS > 1 ? C::NCONS - 1 : 1)][C::NSTATE * 32];
     // CUDA-core path: softmax weights
     alignas(16) float pbuf[C::kMma ? 1 : C::NCONS][C::kMma ? 1 : C::HCAP][C::kMma ? 1 : C::BS];
@@ -178,6 +179,7 @@ struct alignas(1024) DecodeSmem {
     uint64_t empty[C::NSTAGE];
     uint64_t qfull[C::NQ];
     uint64_t qempty[C::NQ];
+    uint64_t xfree;                // the leaders of a unit are done with the state slots
     UnitDesc unit[C::NQ];
     uint32_t issued[C::NSTAGE];    // tiles issued into each stage (producer)
     uint32_t consumed[C::NSTAGE];  // tiles consumed from each stage (consumers)
@@ -984,6 +986,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             sm.issued[i] = 0;
             sm.consumed[i] = 0;
         }
+        mbar_init(&sm.xfree, 1);   // the unit's leader (kernels with one row group)
         for (int i = 0; i < C::NQ; ++i) {
             mbar_init(&sm.qfull[i], 1);
             mbar_init(&sm.qempty[i], C::NCONS);
@@ -1214,17 +1217,29 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
         const int TS = C::kMq ? C::NCONS / row_groups : C::NCONS;
         const int rg = C::kMq ? c / TS : 0;
         const int ts = C::kMq ? c - rg * TS : c;
-        uint32_t gtile = 0;   // tiles of all earlier units, counted over every consumer
+        // Tiles go round robin over the tiles of all units (tile k to consumer k % TS of
+        // the row group), and the consumer of a unit's last tile is its leader: it merges
+        // the others' states and writes the result while the others already start on the
+        // next unit, whose first tiles are theirs.  One consumer barrier per unit, after
+        // its tiles, carries every decision to stop (end of work, a timed-out wait, an
+        // abort) to all consumers at once.  A consumer's state slot is free again once
+        // the previous unit's leader has merged it, which it signals on the xfree
+        // barrier; multi-query kernels, whose leaders stage their output in a state slot,
+        // keep a second barrier after the output instead.
+        uint32_t gtile = 0;   // tiles of all earlier units
         for (uint32_t it = 0;; ++it) {
             const uint32_t qs = it % C::NQ, qphase = (it / C::NQ) & 1;
-            const bool ok = mbar_wait_warp(&sm.qfull[qs], qphase);
-            if (!ok && lane == 0) {
+            bool stop = !mbar_wait_warp(&sm.qfull[qs], qphase);
+            if (stop && lane == 0) {
                 flag_error(p.status, PA_DEVERR_TIMEOUT_);
                 sm.abort = 1;
             }
-            if (all_agree(!ok || sm.abort != 0)) break;
+            stop = stop || warp_sees_abort(sm.abort);
             UnitDesc u = sm.unit[qs];
-            if (u.seq < 0) break;
+            if (stop || u.seq < 0) {
+                (void)all_agree(true);   // the unit barrier below, from a consumer that stops
+                break;
+            }
             if constexpr (C::kMq) {   // this consumer's row group
                 u.row0 += rg * C::HCAP;
                 u.nrows = min(C::HCAP, p.rows - u.row0);
@@ -1238,17 +1253,25 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 mbar_arrive(&sm.qempty[qs]);
             }
             cons.reset();
-            const int32_t b0 = u.tok0 / C::BS, b1 = (u.tok1 + C::BS - 1) / C::BS;
-            const int32_t ntiles = b1 - b0;
-            for (int32_t j = ts; j < ntiles; j += TS) {
+            const int32_t b0 = u.tok0 / C::BS;
+            const int32_t ntiles = (u.tok1 + C::BS - 1) / C::BS - b0;
+            // (multi-query kernels, whose row-group size is a run-time value, keep consumer 0
+            // of the group as leader and start each unit with it)
+            const int gmod = C::kMq ? 0 : (int)(gtile % (uint32_t)TS);
+            const int lead = C::kMq ? 0 : (gmod + ntiles - 1 + TS) % TS;
+            for (int32_t j = (ts - gmod + TS) % TS; j < ntiles; j += TS) {
                 const uint32_t k = gtile + (uint32_t)j;
                 const uint32_t stage = k % C::NSTAGE, fphase = (k / C::NSTAGE) & 1;
-                if (warp_sees_abort(sm.abort)) break;
+                if (warp_sees_abort(sm.abort)) {
+                    stop = true;
+                    break;
+                }
                 if (!mbar_wait_warp(&sm.full[stage], fphase)) {
                     if (lane == 0) {
                         flag_error(p.status, PA_DEVERR_TIMEOUT_);
                         sm.abort = 1;
                     }
+                    stop = true;
                     break;
                 }
                 const int tile0 = (b0 + j) * C::BS;
@@ -1267,21 +1290,35 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 }
             }
             gtile += (uint32_t)ntiles;
-            if constexpr (C::NCONS > 1) {
-                if (ts > 0) cons.export_state(sm.xbuf[c - 1], lane);
-                (void)consumers_any(false, kConsThreads);   // states are in shared memory
-                if (ts == 0) {
-                    for (int o = 1; o < TS; ++o) cons.merge_state(sm.xbuf[c + o - 1], lane);
+            // the row group's state slots: consumer ts exports to slot (ts - lead - 1) mod TS
+            const int xbase = C::kMq ? rg * TS : 0;
+            if (TS > 1 && !stop && ts != lead) {
+                if (!C::kMq && it > 0 && !mbar_wait_warp(&sm.xfree, (it - 1) & 1)) {
+                    if (lane == 0) {
+                        flag_error(p.status, PA_DEVERR_TIMEOUT_);
+                        sm.abort = 1;
+                    }
+                    stop = true;
+                } else {
+                    cons.export_state(sm.xbuf[xbase + (C::kMq ? ts - 1 : (ts - lead - 1 + TS) % TS)], lane);
                 }
             }
-            // A row group's leader stages its output in its own xbuf slot (multi-query):
-            // that slot belongs to the next consumer of the group, whose state the leader
-            // has just merged, or to no one when the group has one consumer.  The slot
-            // holds NSTATE * 32 >= HCAP * D floats.
-            if (ts == 0 && has_rows && !warp_sees_abort(sm.abort))
-                cons.finish(C::kMq ? sm.xbuf[c] : sm.ostage, p, u, lane);
-            // also frees xbuf for the next unit
-            if (all_agree(sm.abort != 0)) break;
+            if (all_agree(stop)) break;   // the unit barrier (also: the states are in shared memory)
+            if (ts == lead) {
+                for (int o = 0; o < TS - 1; ++o) cons.merge_state(sm.xbuf[xbase + o], lane);
+                if (!C::kMq && TS > 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.xfree);
+                }
+                // A row group's leader stages its output in the group's first state slot
+                // (multi-query), whose state it has just merged, or in its own slot when
+                // the group has one consumer.  A slot holds NSTATE * 32 >= HCAP * D floats.
+                if (has_rows && !warp_sees_abort(sm.abort))
+                    cons.finish(C::kMq ? sm.xbuf[xbase] : sm.ostage, p, u, lane);
+            }
+            // multi-query: the leaders' staged outputs leave the slots before the next
+            // unit's states arrive
+            if constexpr (C::kMq) (void)all_agree(false);
         }
     }
 

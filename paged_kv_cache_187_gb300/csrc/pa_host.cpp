@@ -288,7 +288,9 @@ pa::KernelKey kernel_key(const DecodeArgs& a) {
         k.mq_consumers = mq_consumers(a.q_len * g);
         return k;
     }
-    k.mma = g >= 2 && (g > 8 || g_gqa_mma);
+    // fp8 caches take the tensor cores for multi-head attention too: widening E4M3 tiles
+    // to fp16 fragments is cheaper there than per-element conversion on the CUDA cores
+    k.mma = (g >= 2 || a.kv8) && (g > 8 || g_gqa_mma);
     if (k.mma) k.heads_cap = g <= 8 ? 8 : 16;
     else k.heads_cap = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
     k.tile_blocks = tile_blocks_for(a);

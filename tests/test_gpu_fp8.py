@@ -50,15 +50,23 @@ def _batch(dev, lens, Hq, Hkv, bs, dtype, seed):
 
 
 CASES = [
-    ("bf16", 32, 8, 16),    # GQA 4, tensor cores
+    ("bf16", 32, 8, 16),    # GQA 4
     ("bf16", 64, 8, 32),    # GQA 8, 32-token blocks
-    ("f16", 16, 16, 16),    # MHA, CUDA cores
-    ("bf16", 16, 1, 16),    # GQA 16 (two n-tiles)
+    ("f16", 16, 16, 16),    # MHA
+    ("bf16", 16, 1, 16),    # GQA 16 (two n-tiles; tensor cores either way)
 ]
 
 
+@pytest.fixture(params=[True, False], ids=["tensor_cores", "cuda_cores"])
+def fp8_path(request):
+    import paged_kv_cache_187_gb300 as pa
+    pa.pa_set_gqa_tensor_cores(request.param)
+    yield request.param
+    pa.pa_set_gqa_tensor_cores(True)
+
+
 @pytest.mark.parametrize("dtype,Hq,Hkv,bs", CASES)
-def test_fp8_cache_scatter_bit_exact_and_decode(cuda_device, dtype, Hq, Hkv, bs):
+def test_fp8_cache_scatter_bit_exact_and_decode(cuda_device, fp8_path, dtype, Hq, Hkv, bs):
     import paged_kv_cache_187_gb300 as pa
     lens = [1, bs - 1, bs, bs + 1, 100, 257, 511, 513, 1500, 3000]
     b = _batch(cuda_device, lens, Hq, Hkv, bs, dtype, seed=31 + Hq + bs)
