@@ -131,6 +131,9 @@ __device__ __forceinline__ int32_t block_excl_scan(int32_t x, int32_t* buf, int3
 }
 
 constexpr int kTailBuckets = 256;
+// Batches up to this many sequences keep their (clamped) context lengths in shared
+// memory across the plan's passes, so that each is read from global memory once.
+constexpr int kPlanLenCache = 4096;
 
 // Adaptive partitioning aims at this many work units per persistent CTA: enough for the
 // longest-first order to even out the CTAs' finishing times, few enough that most
@@ -152,22 +155,33 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     __shared__ int32_t bstart[kTailBuckets];
     __shared__ unsigned long long total_tokens;
     __shared__ int32_t P_s;
+    __shared__ int32_t len_s[kPlanLenCache];
     allow_dependent_launch();   // the decode kernel may set up meanwhile (it waits for us)
     const int32_t tid = threadIdx.x;
     const int32_t bs = p.block_size;
     for (int32_t i = tid; i < kTailBuckets; i += blockDim.x) hist[i] = 0;
     if (tid == 0) total_tokens = 0ull;
     __syncthreads();
-    // pass 0: the partition size.  Fixed (pa_decode_v2), or adaptive: the largest
-    // multiple of block_size, not below the given minimum, that still yields about
-    // PA_UNITS_PER_CTA units per CTA.
-    if (p.adaptive) {
+    // pass 0: every context length (clamped, errors reported), and the partition size.
+    // Fixed (pa_decode_v2), or adaptive: the largest multiple of block_size, not below
+    // the given minimum, that still yields about PA_UNITS_PER_CTA units per CTA.
+    const bool cached = p.num_seqs <= kPlanLenCache;
+    auto len_of = [&](int32_t s) { return cached ? len_s[s] : clamp_len(p, s, false); };
+    {
         unsigned long long mine = 0;
-        for (int32_t s = tid; s < p.num_seqs; s += blockDim.x) mine += (unsigned)clamp_len(p, s, false);
+        for (int32_t s = tid; s < p.num_seqs; s += blockDim.x) {
+            const int32_t L = clamp_len(p, s, true);
+            if (cached) len_s[s] = L;
+            mine += (unsigned)L;
+        }
+        if (p.adaptive) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-        if ((tid & 31) == 0) atomicAdd(&total_tokens, mine);   // one shared atomic per warp
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            if ((tid & 31) == 0) atomicAdd(&total_tokens, mine);   // one shared atomic per warp
+        }
         __syncthreads();
+    }
+    if (p.adaptive) {
         if (tid == 0) {
             const unsigned long long work =
                 total_tokens * (unsigned long long)p.num_kv_heads * (unsigned long long)p.row_chunks;
@@ -188,7 +202,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         const int32_t s = base + tid;
         int32_t np = 0, nf = 0;
         if (s < p.num_seqs) {
-            const int32_t L = clamp_len(p, s, true);
+            const int32_t L = len_of(s);
             nf = L / P;
             const int32_t tail = L - nf * P;
             np = nf + ((tail > 0 || L == 0) ? 1 : 0);
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         const int32_t s = base + tid;
         int32_t np = 0, nf = 0, L = 0, tail = 0;
         if (s < p.num_seqs) {
-            L = clamp_len(p, s, false);
+            L = len_of(s);
             nf = L / P;
             tail = L - nf * P;
             np = nf + ((tail > 0 || L == 0) ? 1 : 0);

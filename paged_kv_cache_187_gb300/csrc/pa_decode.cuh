@@ -1072,9 +1072,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
         // The first unit.  Later units are claimed one ahead: the atomic, the list entry
         // and the first block-table entries of unit k+1 are fetched while unit k's tiles
         // are issued, so that a new unit does not start with three dependent loads.
-        int32_t claimed = 0;   // lane 0: raw result of the last atomic claim
-        if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
-        int32_t w = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : (int32_t)blockIdx.x;
+        // Every CTA starts with the unit of its own index (no claim to wait for); the
+        // units after the first gridDim.x are claimed from the counter.
+        int32_t claimed = 0;   // lane 0: the unit of the last atomic claim
+#ifndef PA_STATIC_FIRST_UNIT
+#define PA_STATIC_FIRST_UNIT 1
+#endif
+        const uint32_t claim_base = PA_STATIC_FIRST_UNIT ? gridDim.x : 0u;
+        if (!PA_STATIC_FIRST_UNIT && persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+        int32_t w = (PA_STATIC_FIRST_UNIT || !persistent) ? (int32_t)blockIdx.x : __shfl_sync(0xffffffffu, claimed, 0);
         int4 e = (persistent && w < total) ? p.part_list[w / upl] : kNoEntry;
         int32_t pre_phys = 0;       // prefetched first block-table chunk of unit w
         bool have_pre = false;
@@ -1130,7 +1136,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             int step = 0;
             auto advance_next = [&]() {
                 if (step == 0) {
-                    if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+                    if (persistent && lane == 0)
+                        claimed = (int32_t)(claim_base + atomicAdd(&p.hdr->counter, 1u));
                     step = 1;
                 } else if (step == 1) {
                     w_next = persistent ? __shfl_sync(0xffffffffu, claimed, 0) : total;

@@ -263,12 +263,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // The next unit is claimed as soon as the current one is published and its list
         // entry is read after the current unit's first tile, so neither round trip stalls
         // the tile stream.
+        // every CTA starts with the unit of its own index; later units are claimed from the
+        // counter, past the first gridDim.x
         int32_t w = (int32_t)blockIdx.x;
-        if (persistent) {
-            int32_t claimed = 0;
-            if (lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
-            w = __shfl_sync(0xffffffffu, claimed, 0);
-        }
         int4 e = (persistent && w < total) ? p.part_list[w / upl] : kNoEntry;
         uint32_t kt = 0;   // tiles issued into the K ring
         bool ok = true;
@@ -317,7 +314,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 q_staged = true;
             };
             int32_t claimed = total;
-            if (persistent && lane == 0) claimed = (int32_t)atomicAdd(&p.hdr->counter, 1u);
+            if (persistent && lane == 0) claimed = (int32_t)(gridDim.x + atomicAdd(&p.hdr->counter, 1u));
             int32_t w_next = total;
             int4 e_next = kNoEntry;
             bool have_next = false;

@@ -10,9 +10,9 @@
 namespace pa {
 
 // Head of the V2 workspace.  The plan kernel writes it; the decode kernel's persistent
-// CTAs claim work units from `counter`.
+// CTAs start with the unit of their own index and claim the later ones from `counter`.
 struct WsHeader {
-    uint32_t counter;         // next unclaimed work unit
+    uint32_t counter;         // units claimed so far past the first gridDim.x
     uint32_t total_units;     // partitions * num_kv_heads * row_chunks
     uint32_t total_parts;     // partitions over all sequences
     uint32_t partition_size;  // tokens per partition used by this call
