@@ -469,6 +469,55 @@ def run_e2e(args, w, device, rank, pa, W, DecodeRunner):
                     "for each step's output before reusing its buffers (ring of 3); wall clock"}
 
 
+def run_multistep_case(args):
+    """The k-step decode loop of one workload on the device (per step: pa_advance_step,
+    reshape_and_cache of the step's new tokens, decode), timed with CUDA events as issued
+    from Python and as one CUDA-graph replay.  Prints the whole loop's time and the mean
+    per step; bytes per step are the decode's algorithmic bytes at that step's lengths."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_187_gb300 import workloads as W
+    from paged_kv_cache_187_gb300.runner import DecodeRunner
+    w = W.WORKLOADS[args.profile_workload]
+    k = args.multistep
+    r = DecodeRunner(w, device="cuda").setup_multistep(k)
+    lens0 = r.ms_lens0.astype(np.int64)
+    kv_per_token = w.num_kv_heads * w.head_size * 2 * 2
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_size * 2
+    tokens = sum(int((lens0 + j + 1).sum()) for j in range(k))
+    loop_bytes = tokens * kv_per_token + k * qo
+    r.run_multistep()
+    torch.cuda.synchronize()
+    graph = r.capture_multistep()
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sorted(a.elapsed_time(b) for a, b in evs)
+
+    for _ in range(args.warmup):
+        r.run_multistep()
+        graph.replay()
+    torch.cuda.synchronize()
+    res = {}
+    for name, fn in (("eager", r.run_multistep), ("graph", graph.replay)):
+        t = timed(fn, args.steps)
+        ms = t[len(t) // 2]
+        res[name] = {"loop_ms": ms, "us_per_step": 1e3 * ms / k,
+                     "GBps": loop_bytes / (ms * 1e-3) / 1e9,
+                     "seq_tokens_per_s": tokens / (ms * 1e-3)}
+    assert int(r.status.item()) == 0
+    print(json.dumps({"multistep_case": w.name, "steps_per_loop": k, "loops_timed": args.steps,
+                      "warmup": args.warmup, "loop_bytes": loop_bytes, "loop_seq_tokens": tokens,
+                      "step": "pa_advance_step + pa_decode_step (reshape_and_cache + auto decode)",
+                      **res}))
+
+
 def run_profile_case(args):
     """Small, self-contained case for ncu: decode steps of one workload only."""
     import torch
@@ -533,9 +582,15 @@ def main():
                     help="profile case: keep the KV pools in fp8 E4M3")
     ap.add_argument("--q-len", type=int, default=1,
                     help="profile case: multi-query decode with this many query tokens per sequence")
+    ap.add_argument("--multistep", type=int, default=0,
+                    help="with --profile-workload: time the k-step device loop (eager and "
+                         "as a CUDA graph)")
     args = ap.parse_args()
     if args.profile_workload:
-        run_profile_case(args)
+        if args.multistep > 0:
+            run_multistep_case(args)
+        else:
+            run_profile_case(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -399,7 +399,13 @@ cudaError_t launch_plan(const DecodeParams& p, cudaStream_t stream) {
     // is no longer in use when it does.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(1024);
+    // one thread per sequence, between kTailBuckets (the bucket scan takes one thread per
+    // bucket) and 1024
+#ifndef PA_PLAN_MIN_THREADS
+#define PA_PLAN_MIN_THREADS kTailBuckets
+#endif
+    const int32_t want = (p.num_seqs + 31) / 32 * 32;
+    cfg.blockDim = dim3((unsigned)std::min(1024, std::max((int32_t)PA_PLAN_MIN_THREADS, want)));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
