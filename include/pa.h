@@ -186,10 +186,13 @@ pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* key
 
 /* pa_decode_fp8: paged decode over fp8 pools: out = softmax(scale * q . (k_scale * k_t))
  * (v_scale * v_t), query and out fp16 or bf16 (`dtype`), head_size 128.  variant 0 =
- * pa_decode_auto's choice, 1 = V1, 2 = V2 with `partition_size`; workspace as for
- * those (the same *_workspace_size calls apply).  Internally the K / V tiles are
- * widened to fp16 (exact) and the query rounded to fp16, so queries beyond fp16's range
- * (|q| > 65504) are not supported. */
+ * pa_decode_auto's choice, 1 = V1, 2 = V2 with `partition_size` (a multiple of
+ * block_size); workspace as for those (the same *_workspace_size calls apply).
+ * Internally the K / V tiles are widened to fp16 (exact); on the tensor-core path (the
+ * default, see pa_set_gqa_tensor_cores) the query is rounded to fp16, so queries beyond
+ * fp16's range (|q| > 65504) are not supported there.  With 16-token blocks the kernel
+ * takes two blocks per step when partitions are multiples of 32 tokens (V1, auto, or
+ * such a partition_size), one block otherwise; results meet the same tolerance. */
 pa_status pa_decode_fp8(void* out, const void* query, const void* key_cache, const void* value_cache,
                         const int32_t* block_tables, int32_t max_blocks_per_seq,
                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
