@@ -13,18 +13,20 @@
 // separate reduction launch is needed.
 //
 // GB300 design (one CTA = 1 producer warp + NCONS consumer warps, several CTAs per SM):
-//   * the producer claims work units, copies the unit's query rows with a 1-D bulk copy,
-//     and streams the unit's K and V tiles -- one (block, kv head) tile is block_size x
-//     head_size contiguous elements -- with 2-D tensor TMA into an NSTAGE-deep ring of
-//     shared-memory stages (128-byte swizzle, L2 evict-first);
-//   * consumer c takes tiles c, c + NCONS, ... of each unit and runs the online softmax
-//     over them; the consumers' states are merged through shared memory at the end of
-//     the unit:
-//       - group >= 2 (GQA): S^T = K_tile Q^T and O^T += V_tile^T P^T on the tensor cores
-//         (mma.sync m16n8k16, tokens / head dims on M, the group's query heads on N),
-//         P moved from accumulator to operand layout with movmatrix;
-//       - group 1 (MHA) or on request: CUDA cores, each lane owning head_size/32 dims,
-//         dot products finished by a transposed butterfly reduction;
+//   * the producer takes work units, copies the unit's query rows with a 1-D bulk copy,
+//     and streams the unit's K and V tiles -- a (block, kv head) box is block_size x
+//     head_size contiguous elements; an fp8 tile over 16-token blocks holds two -- with
+//     2-D tensor TMA into an NSTAGE-deep ring of shared-memory stages (128-byte swizzle,
+//     L2 evict-first);
+//   * the consumers take the tiles round robin and run the online softmax over them; at
+//     the end of a unit the consumer of its last tile merges the others' states (through
+//     shared memory) and writes the result while the others start the next unit:
+//       - group >= 2 (GQA), and fp8 caches: S^T = K_tile Q^T and O^T += V_tile^T P^T on
+//         the tensor cores (mma.sync m16n8k16, tokens / head dims on M, the group's
+//         query heads on N), P moved from accumulator to operand layout with movmatrix;
+//         fp8 tiles are widened to fp16 fragments in registers;
+//       - group 1 (MHA) over a 16-bit cache, or on request: CUDA cores, each lane owning
+//         head_size/32 dims, dot products finished by a transposed butterfly reduction;
 //       - several query tokens per sequence (multi-query, to verify speculative
 //         tokens): the tensor-core path with (query token, head) pairs on N, each
 //         column masked causally at its own token limit;
@@ -1217,17 +1219,18 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
             else return __any_sync(0xffffffffu, v);
         };
         Consumer cons;
-        // Tile split and row group of this consumer: the consumers of a row group share
-        // the unit's tiles round robin (ts = 0 .. TS-1); ordinary kernels have one row
-        // group, so TS = NCONS.  NSTAGE is a multiple of TS, so a stage is always used by
-        // the same consumers.
+        // Row group of this consumer and its place in the group (ts = 0 .. TS-1): the
+        // consumers of a row group share its tiles; ordinary kernels have one row group,
+        // so TS = NCONS.
         const int TS = C::kMq ? C::NCONS / row_groups : C::NCONS;
         const int rg = C::kMq ? c / TS : 0;
         const int ts = C::kMq ? c - rg * TS : c;
-        // Tiles go round robin over the tiles of all units (tile k to consumer k % TS of
-        // the row group), and the consumer of a unit's last tile is its leader: it merges
-        // the others' states and writes the result while the others already start on the
-        // next unit, whose first tiles are theirs.  One consumer barrier per unit, after
+        // Tiles go round robin over the tiles of all units (tile k to consumer k % TS; as
+        // NSTAGE is a multiple of TS, a stage always serves the same consumer), and the
+        // consumer of a unit's last tile is its leader: it merges the others' states and
+        // writes the result while the others already start on the next unit, whose first
+        // tiles are theirs.  Multi-query kernels deal each unit's tiles from consumer 0 of
+        // the group, which leads.  One consumer barrier per unit, after
         // its tiles, carries every decision to stop (end of work, a timed-out wait, an
         // abort) to all consumers at once.  A consumer's state slot is free again once
         // the previous unit's leader has merged it, which it signals on the xfree

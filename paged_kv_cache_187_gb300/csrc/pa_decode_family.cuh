@@ -74,10 +74,12 @@ constexpr int decode_min_ctas() {
 // MQC: consumer warps of a multi-query kernel (kMqConsumersNarrow or kMqConsumersWide).
 template <bool MMA, int BS, bool KV8, int MQC = 0>
 constexpr int consumers_for() {
-    // fp8 tiles carry twice the tokens per byte, so their consumers do about four times
-    // the work per byte of a 16-bit tile.  Measured on the Llama-3-8B / -70B batches, the
-    // tensor-core path does best with 2 consumer warps for 16-token blocks (4 CTAs per SM
-    // at 144 registers) and 3 for 32-token blocks; the CUDA-core path with 3.
+    // fp8 tiles carry twice the tokens per byte, so their consumers do more work per byte
+    // than those of a 16-bit tile.  Measured on the Llama-3-8B / -70B batches, the
+    // tensor-core path does best with 3 consumer warps for 32-token tiles (32-token
+    // blocks, or two 16-token blocks; 2 and 4 were slower) and 2 for single 16-token
+    // blocks (partitions that are not a multiple of 32 tokens); the CUDA-core path with 3.
+    // BS here is the tile's token count.
     if (KV8) return MMA ? PA_FP8_MMA_CONSUMERS(BS) : PA_FP8_CORE_CONSUMERS;
     if (MQC) return MQC;
     return MMA ? PA_MMA_CONSUMERS(BS) : PA_CORE_CONSUMERS;
