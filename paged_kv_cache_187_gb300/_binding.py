@@ -500,10 +500,14 @@ def pa_selftest_wait_timeout(status, limit_us: int, stream=None):
 
 
 def pa_set_gqa_tensor_cores(enable: bool):
+    """Process-wide: True (default) decodes grouped-query heads and fp8 caches on the
+    tensor cores, False on the CUDA cores (groups above 8 stay on the tensor cores)."""
     _check(_lib.pa_set_gqa_tensor_cores(1 if enable else 0))
 
 
 def pa_set_mq_tcgen05(enable: bool):
+    """Process-wide: True (default) lets multi-query decode with many rows per kv head
+    use the tcgen05 kernel, False keeps it on the mma.sync kernel."""
     _check(_lib.pa_set_mq_tcgen05(1 if enable else 0))
 
 
