@@ -31,8 +31,10 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+# PA_ORACLE_SRC points the wrapper at another copy of oracle.c (the planted-mistake
+# tests compile altered copies in a scratch folder); the library is built next to it.
+_SRC = os.environ.get("PA_ORACLE_SRC") or os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(_SRC)), "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
