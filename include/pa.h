@@ -46,6 +46,19 @@
  *     the block-table row, a pipeline wait that exceeded its time limit) never fault:
  *     the offending access is skipped, and if `status_dev` is not NULL the kernel ORs
  *     the matching PA_DEVERR_* bit into that device int32.
+ *
+ * A typical decode step (one layer, one new token per running sequence)
+ *   host    pa_alloc_append_batch        the slot of each sequence's new token (a new
+ *                                        block is popped when the last one is full)
+ *           pa_alloc_block_tables,       the tables and lengths, copied to the device
+ *           pa_alloc_context_lens        with the slots
+ *   device  pa_reshape_and_cache         the new K / V rows into the pools by slot
+ *           pa_decode_auto               out <- attention of each query over its
+ *                                        sequence's pooled tokens (workspace of
+ *                                        pa_decode_auto_workspace_size bytes)
+ *   pa_decode_step issues both device calls at once; pa_decode_step_host also copies
+ *   the step's inputs from host memory and the output back; pa_advance_step moves the
+ *   lengths and slots on the device between the steps of a multi-step loop.
  */
 #ifndef PA_H_
 #define PA_H_
