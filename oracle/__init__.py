@@ -219,8 +219,12 @@ def reshape_and_cache_fp8(key_bits, value_bits, key_cache8, value_cache8, slot_m
 
 
 def decode_fp8(q_bits, k_cache8, v_cache8, block_tables, context_lens, scale, k_scale, v_scale,
-               dtype, only=None) -> np.ndarray:
-    """Exact fp64 decode over fp8 E4M3 pools (dequantised by the per-tensor scales)."""
+               dtype, only=None, strict: bool = True):
+    """Exact fp64 decode over fp8 E4M3 pools (dequantised by the per-tensor scales).
+
+    A token whose block the table does not give (its logical block past the table row,
+    or an entry outside the pool) reads as zeros.  strict=True raises IndexError when
+    that happened; strict=False returns (out, flagged) instead."""
     lib = _load()
     q = _c(q_bits, np.uint16)
     kc = _c(k_cache8, np.uint8)
@@ -237,6 +241,8 @@ def decode_fp8(q_bits, k_cache8, v_cache8, block_tables, context_lens, scale, k_
                                  _ptr(only_arr) if only_arr is not None else None)
     if rc == -2:
         raise ValueError("oracle: unsupported shapes")
+    if not strict:
+        return out, rc == -1
     if rc == -1:
         raise IndexError("oracle: block table entry outside the pool")
     return out

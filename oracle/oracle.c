@@ -222,12 +222,12 @@ static double cache_at(const decode_args* a, const uint16_t* cache, int32_t s,
     return widen(cache[idx], a->dtype);
 }
 
-/* Scaled dot products l_t = scale * sum_d q_d k_t,d for tokens [t0, t1). */
-static void logits_range(const decode_args* a, int32_t s, int32_t h, int32_t t0, int32_t t1,
-                         double* logit, int* bad) {
+/* Scaled dot products l_t = scale * sum_d q_d k_t,d for tokens [t0, t1), q_d being
+ * element d of the query row `qrow` of query head h. */
+static void logits_range(const decode_args* a, const uint16_t* qrow, int32_t s, int32_t h,
+                         int32_t t0, int32_t t1, double* logit, int* bad) {
     int32_t group = a->num_q_heads / a->num_kv_heads;
     int32_t kvh = h / group;
-    const uint16_t* qrow = a->q + ((int64_t)s * a->num_q_heads + h) * a->head_size;
     for (int32_t t = t0; t < t1; ++t) {
         double acc = 0.0;
         for (int32_t d = 0; d < a->head_size; ++d)
@@ -236,15 +236,17 @@ static void logits_range(const decode_args* a, int32_t s, int32_t h, int32_t t0,
     }
 }
 
-/* Softmax-weighted sum of V over tokens [t0, t1) for query head h:
+/* Softmax-weighted sum of V over tokens [t0, t1) of sequence s for query head h, whose
+ * query row is `qrow`:
  *   m = max l_t,  p_t = exp(l_t - m),  l = sum p_t,  o = sum p_t v_t / l.
  * Writes o (head_size values) and returns m and l through the pointers. */
-static void attend_range(const decode_args* a, int32_t s, int32_t h, int32_t t0, int32_t t1,
-                         double* o, double* m_out, double* l_out, double* scratch, int* bad) {
+static void attend_range(const decode_args* a, const uint16_t* qrow, int32_t s, int32_t h,
+                         int32_t t0, int32_t t1, double* o, double* m_out, double* l_out,
+                         double* scratch, int* bad) {
     int32_t group = a->num_q_heads / a->num_kv_heads;
     int32_t kvh = h / group;
     int32_t n = t1 - t0;
-    logits_range(a, s, h, t0, t1, scratch, bad);
+    logits_range(a, qrow, s, h, t0, t1, scratch, bad);
     double m = -INFINITY;
     for (int32_t i = 0; i < n; ++i) if (scratch[i] > m) m = scratch[i];
     double l = 0.0;
@@ -294,8 +296,9 @@ int32_t or_paged_decode_v1(double* out, const uint16_t* q, const uint16_t* k_cac
                 for (int32_t d = 0; d < head_size; ++d) o[d] = 0.0;
                 continue;
             }
+            const uint16_t* qrow = q + ((int64_t)s * num_q_heads + h) * head_size;
             double m, l;
-            attend_range(&a, s, h, 0, L, o, &m, &l, scratch, &bad);
+            attend_range(&a, qrow, s, h, 0, L, o, &m, &l, scratch, &bad);
         }
         free(scratch);
     }
@@ -337,10 +340,11 @@ int32_t or_paged_decode_v2(double* out, const uint16_t* q, const uint16_t* k_cac
                 for (int32_t d = 0; d < head_size; ++d) o[d] = 0.0;
                 continue;
             }
+            const uint16_t* qrow = q + ((int64_t)s * num_q_heads + h) * head_size;
             for (int32_t p = 0; p < np; ++p) {
                 int32_t t0 = p * partition_size;
                 int32_t t1 = t0 + partition_size < L ? t0 + partition_size : L;
-                attend_range(&a, s, h, t0, t1, op + (int64_t)p * head_size, &mp[p], &lp[p],
+                attend_range(&a, qrow, s, h, t0, t1, op + (int64_t)p * head_size, &mp[p], &lp[p],
                              scratch, &bad);
             }
             double M = -INFINITY;
@@ -392,12 +396,10 @@ int32_t or_paged_decode_mq(double* out, const uint16_t* q, const uint16_t* k_cac
                     for (int32_t d = 0; d < head_size; ++d) o[d] = 0.0;
                     continue;
                 }
-                /* the row's own query: a view of q with the multi-query layout */
-                decode_args aj = a;
-                aj.q = q + ((int64_t)s * q_len + j) * num_q_heads * head_size
-                         - (int64_t)s * num_q_heads * head_size;
+                /* the query row of new token j, head h */
+                const uint16_t* qrow = q + (((int64_t)s * q_len + j) * num_q_heads + h) * head_size;
                 double m, l;
-                attend_range(&aj, s, h, 0, limit, o, &m, &l, scratch, &bad);
+                attend_range(&a, qrow, s, h, 0, limit, o, &m, &l, scratch, &bad);
             }
         }
         free(scratch);
@@ -441,8 +443,23 @@ int32_t or_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, uin
     return bad;
 }
 
+/* Offset of the row of token t (sequence s, kv head kvh) in a pool laid out
+ * [num_blocks][num_kv_heads][block_size][head_size], found through the block table; -1
+ * (and *bad set) when t's logical block lies past the sequence's table row or the entry
+ * lies outside the pool.  Such a token reads as zeros, the same reading as cache_at. */
+static int64_t pool_row(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        int32_t num_kv_heads, int32_t block_size, int32_t head_size,
+                        int32_t num_blocks, int32_t s, int32_t kvh, int32_t t, int* bad) {
+    int32_t logical = t / block_size;
+    if (logical >= max_blocks_per_seq) { *bad = 1; return -1; }
+    int32_t phys = block_tables[(int64_t)s * max_blocks_per_seq + logical];
+    if (phys < 0 || phys >= num_blocks) { *bad = 1; return -1; }
+    return (((int64_t)phys * num_kv_heads + kvh) * block_size + t % block_size) * head_size;
+}
+
 /* Decode over an fp8 cache: the plain definition with k_t = decode(K8) * k_scale and
- * v_t = decode(V8) * v_scale, everything else as or_paged_decode_v1. */
+ * v_t = decode(V8) * v_scale, everything else as or_paged_decode_v1 (a token whose block
+ * the table does not give reads as zeros: logit 0, no V contribution; return -1). */
 int32_t or_paged_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_cache,
                             const uint8_t* v_cache, const int32_t* block_tables,
                             int32_t max_blocks_per_seq, const int32_t* context_lens,
@@ -464,25 +481,22 @@ int32_t or_paged_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_cac
             const uint16_t* qrow = q + ((int64_t)s * num_q_heads + h) * head_size;
             double m = -INFINITY;
             for (int32_t t = 0; t < L; ++t) {
-                int32_t phys = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
-                if (t / block_size >= max_blocks_per_seq || phys < 0 || phys >= num_blocks) {
-                    bad = 1;
-                    p[t] = -INFINITY;
-                    continue;
-                }
-                int64_t row = (((int64_t)phys * num_kv_heads + kvh) * block_size + t % block_size) * head_size;
+                int64_t row = pool_row(block_tables, max_blocks_per_seq, num_kv_heads, block_size,
+                                       head_size, num_blocks, s, kvh, t, &bad);
                 double acc = 0.0;
-                for (int32_t d = 0; d < head_size; ++d)
-                    acc += widen(qrow[d], dtype) * (or_e4m3_to_f64(k_cache[row + d]) * (double)k_scale);
+                if (row >= 0)
+                    for (int32_t d = 0; d < head_size; ++d)
+                        acc += widen(qrow[d], dtype) *
+                               (or_e4m3_to_f64(k_cache[row + d]) * (double)k_scale);
                 p[t] = (double)scale * acc;
                 if (p[t] > m) m = p[t];
             }
             double l = 0.0;
             for (int32_t t = 0; t < L; ++t) { p[t] = exp(p[t] - m); l += p[t]; }
             for (int32_t t = 0; t < L; ++t) {
-                int32_t phys = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
-                if (phys < 0 || phys >= num_blocks) continue;
-                int64_t row = (((int64_t)phys * num_kv_heads + kvh) * block_size + t % block_size) * head_size;
+                int64_t row = pool_row(block_tables, max_blocks_per_seq, num_kv_heads, block_size,
+                                       head_size, num_blocks, s, kvh, t, &bad);
+                if (row < 0) continue;
                 for (int32_t d = 0; d < head_size; ++d)
                     o[d] += p[t] * (or_e4m3_to_f64(v_cache[row + d]) * (double)v_scale);
             }

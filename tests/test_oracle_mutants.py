@@ -28,6 +28,8 @@ MUTANTS = [
      "int32_t limit = L - q_len + j;", 1, "multi_query"),
     ("fp8_dropped_v_scale", "(or_e4m3_to_f64(v_cache[row + d]) * (double)v_scale)",
      "or_e4m3_to_f64(v_cache[row + d])", 1, "fp8_cache_decode"),
+    ("fp8_table_row_bound", "    if (logical >= max_blocks_per_seq) { *bad = 1; return -1; }\n", "", 1,
+     "fp8_decode_context_past"),
     ("ties_away_16bit", "double r = nearbyint(n);              /* default rounding mode: ties to even */",
      "double r = round(n);", 1, "rounding and not e4m3"),
     ("ties_away_e4m3", "    double r = nearbyint(n);\n    if (r >= 16.0)",

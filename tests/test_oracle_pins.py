@@ -488,6 +488,43 @@ def test_fp8_cache_decode_equals_dense_attention_over_dequantised_values():
         np.testing.assert_allclose(got[s], np.einsum("ht,thd->hd", p, v), rtol=1e-12, atol=1e-13)
 
 
+def test_fp8_decode_context_past_its_table_row_reads_zeros_and_flags():
+    """A context longer than its block-table row: the tokens past the row have no block,
+    so they read as zeros (logit 0, no V contribution) and the call is flagged -- the
+    same reading as the 16-bit decode and the GPU (an out-of-pool tile reads as zeros).
+    The entry that physically follows the row belongs to the next sequence and points at
+    a NaN-poisoned block; reading it would turn the output into NaN."""
+    D, bs, Hq, Hkv = 32, 16, 4, 2
+    rng = np.random.default_rng(23)
+    ks, vs = np.float32(0.05), np.float32(0.04)
+    nb = 3
+    kc = np.full((nb, Hkv, bs, D), 0x7F, np.uint8)     # E4M3 NaN everywhere
+    vc = kc.copy()
+    k16 = oracle.round_to(rng.standard_normal((bs, Hkv, D)), "f16")
+    v16 = oracle.round_to(rng.standard_normal((bs, Hkv, D)), "f16")
+    slots = np.arange(2 * bs, 3 * bs, dtype=np.int32)  # block 2 holds sequence 0's 16 tokens
+    assert oracle.reshape_and_cache_fp8(k16, v16, kc, vc, slots, bs, "f16", ks, vs) == 0
+    bt = np.array([[2], [0]], np.int32)                # one block per row; block 0 is poison
+    lens = np.array([bs + 3, 0], np.int32)             # 3 tokens past sequence 0's row
+    q = oracle.round_to(rng.standard_normal((2, Hq, D)), "f16")
+    scale = np.float32(D ** -0.5)
+    got, flagged = oracle.decode_fp8(q, kc, vc, bt, lens, scale, ks, vs, "f16", strict=False)
+    assert flagged and np.all(np.isfinite(got))
+    with pytest.raises(IndexError):
+        oracle.decode_fp8(q, kc, vc, bt, lens, scale, ks, vs, "f16")
+    inv_k, inv_v = np.float32(1) / ks, np.float32(1) / vs
+    def deq(x16, inv, sc):
+        xf = oracle.widen(x16, "f16").astype(np.float32)
+        return oracle.e4m3_widen(oracle.e4m3_round((xf * inv).astype(np.float64))) * float(sc)
+    g = Hq // Hkv
+    k = np.concatenate([np.repeat(deq(k16, inv_k, ks), g, axis=1), np.zeros((3, Hq, D))])
+    v = np.concatenate([np.repeat(deq(v16, inv_v, vs), g, axis=1), np.zeros((3, Hq, D))])
+    logits = np.einsum("hd,thd->ht", oracle.widen(q[0], "f16"), k) * float(scale)
+    ref = np.einsum("ht,thd->hd", scipy.special.softmax(logits, axis=1), v)
+    np.testing.assert_allclose(got[0], ref, rtol=1e-12, atol=1e-13)
+    assert np.all(got[1] == 0)                         # empty context: zero rows
+
+
 # --------------------------------------------------------------------------- multi-query
 def test_multi_query_rows_equal_single_query_decodes_over_their_prefixes():
     D, bs, Hq, Hkv, QL = 16, 8, 4, 2, 3
