@@ -248,7 +248,9 @@ pa_status pa_decode_mq(void* out, const void* query, const void* key_cache, cons
  * query rows (q_len x group) per kv head, or more than 8 with 16-token blocks: 1 (the
  * default) runs it on the 5th-generation tensor cores (tcgen05, accumulators in tensor
  * memory), 0 on mma.sync.  Other shapes, and fixed V2 partition sizes that are not a
- * multiple of 128 tokens, always take the mma.sync kernel.  Process-wide; returns PA_OK. */
+ * multiple of 128 tokens, always take the mma.sync kernel.  The setting belongs to the
+ * calling thread: it changes that thread's later calls only (each thread starts at 1).
+ * Returns PA_OK. */
 pa_status pa_set_mq_tcgen05(int32_t enable);
 
 /* One decode step of the hot path on device buffers: pa_reshape_and_cache of the
@@ -309,7 +311,8 @@ pa_status pa_decode_step_host_overlapped(
  * group: 1 (default) contracts the group's query heads with each K/V tile on the tensor
  * cores (mma.sync m16n8k16, fp32 accumulate); 0 uses the CUDA-core path that
  * multi-head attention over 16-bit caches always takes.  Groups above 8 stay on the
- * tensor cores.  Process-wide; both paths meet the same tolerance. */
+ * tensor cores.  Both paths meet the same tolerance.  The setting belongs to the calling
+ * thread: it changes that thread's later calls only (each thread starts at 1). */
 pa_status pa_set_gqa_tensor_cores(int32_t enable);
 
 /* ------------------------------------------------------------------------------ */
@@ -325,11 +328,15 @@ pa_status pa_set_gqa_tensor_cores(int32_t enable);
  * PA_NOALLOC_SCRATCH_BYTES compiled into the library.  Every GPU that loads the library
  * keeps that array until the process exits.  The caller still passes inputs and outputs.
  *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
- *   - If pa_decode_v2_workspace_size() for the arguments exceeds
+ *   - It checks its arguments as pa_decode_v2 does and returns the same errors; then,
+ *     if pa_decode_v2_workspace_size() for the arguments exceeds
  *     PA_NOALLOC_SCRATCH_BYTES, it returns PA_ERR_WORKSPACE and launches nothing.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
- *     any stream capture begins.
+ *     any stream capture begins.  The address is kept for the life of the process: after
+ *     cudaDeviceReset (or anything else that tears down the device's primary context)
+ *     the library's module is loaded again and the cached address is stale, so do not
+ *     call this entry point on that device again in the same process.
  *   - All calls share the one array and it keeps the last call's contents (each call
  *     rewrites everything it reads).  Calls whose kernels overlap on the GPU -- on two
  *     streams, or from two threads -- race on it and give wrong results; serialise them. */
@@ -379,10 +386,13 @@ pa_status pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* bloc
  * never completes.  The kernel returns normally; the context stays usable. */
 pa_status pa_selftest_wait_timeout(int32_t* status_dev, uint32_t limit_us, pa_stream stream);
 
-/* Profiling hook: when both are non-NULL (cudaEvent_t handles), every later decode
- * call records `start_event` on its stream right before it launches the paged decode
- * kernel and `stop_event` right after, so that the kernel alone can be timed with
- * cudaEventElapsedTime.  NULL, NULL turns the hook off (the default).  Process-wide. */
+/* Profiling hook, for benchmarks and tests; no result depends on it.  When both are
+ * non-NULL (cudaEvent_t handles), every later decode call of the calling thread records
+ * `start_event` on its stream right before it launches the paged decode kernel and
+ * `stop_event` right after, so that the kernel alone can be timed with
+ * cudaEventElapsedTime.  NULL, NULL turns the hook off (each thread starts with it off).
+ * While it is on, the decode kernel no longer starts early under the kernel before it
+ * (the plan or reshape kernel), so a step takes a few microseconds longer. */
 pa_status pa_set_kernel_events(void* start_event, void* stop_event);
 
 /* ------------------------------------------------------------------------------ */

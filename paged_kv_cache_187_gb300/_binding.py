@@ -237,7 +237,18 @@ def pa_decode_v2(out, query, key_cache, value_cache, block_tables, context_lens,
                              _stream(stream)))
 
 
-PA_NOALLOC_SCRATCH_BYTES = 64 << 20
+def _header_scratch_bytes() -> int:
+    """PA_NOALLOC_SCRATCH_BYTES as include/pa.h defines it (the one source of the size)."""
+    import re
+    with open(os.path.join(os.path.dirname(_PKG), "include", "pa.h")) as f:
+        m = re.search(r"#define\s+PA_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)",
+                      f.read())
+    if not m:
+        raise ImportError("include/pa.h: PA_NOALLOC_SCRATCH_BYTES not found")
+    return int(m.group(1)) << int(m.group(2))
+
+
+PA_NOALLOC_SCRATCH_BYTES = _header_scratch_bytes()
 
 
 def pa_decode_v2_noalloc(out, query, key_cache, value_cache, block_tables, context_lens,

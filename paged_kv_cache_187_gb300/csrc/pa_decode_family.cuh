@@ -99,13 +99,15 @@ cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
                         decode_min_ctas<C0>(), BS>;
     constexpr size_t smem = decode_smem_bytes<C>();
     auto kern = paged_decode_kernel<C>;
-    static bool configured = false;   // per instantiation; attribute setting is idempotent
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    // the shared-memory limit is a per-device attribute: set once on each device
+    static PerDeviceOnce configured;
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    e0 = static_cast<cudaError_t>(configured.run(dev, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    }));
+    if (e0 != cudaSuccess) return e0;
     if (ctas_per_sm_out) {
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, smem);

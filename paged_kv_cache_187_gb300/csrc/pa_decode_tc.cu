@@ -12,12 +12,15 @@ cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const De
     constexpr size_t smem = tc::tc_smem_bytes<C>();
     static_assert(smem <= 227 * 1024, "shared memory");
     auto kern = tc::paged_decode_tc_kernel<C>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    // the shared-memory limit is a per-device attribute: set once on each device
+    static PerDeviceOnce configured;
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    e0 = static_cast<cudaError_t>(configured.run(dev, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    }));
+    if (e0 != cudaSuccess) return e0;
     if (occ) {
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, smem);

@@ -50,9 +50,11 @@ struct DeviceInfo {
 std::mutex g_mu;
 std::unordered_map<int, DeviceInfo> g_dev;
 std::unordered_map<uint64_t, int32_t> g_occ;   // (device, kernel key) -> CTAs per SM
-int32_t g_gqa_mma = 1;
-int32_t g_mq_tc = 1;
-cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+// Kernel choices and the profiling events belong to the calling thread: one thread's
+// setting never changes what another thread's calls launch.
+thread_local int32_t g_gqa_mma = 1;
+thread_local int32_t g_mq_tc = 1;
+thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 
 // Launches the decode kernel, bracketed by the profiling events when they are set.
 cudaError_t timed_decode(const pa::KernelKey& k, const CUtensorMap& km, const CUtensorMap& vm,
@@ -425,6 +427,25 @@ void auto_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t block_size,
 }  // namespace
 
 namespace pa {
+
+int32_t check_decode_v2_args(const void* out, const void* query, const void* key_cache,
+                             const void* value_cache, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_size, int32_t block_size, int32_t num_blocks,
+                             int32_t max_context_len, int32_t dtype, int32_t partition_size) {
+    DecodeArgs a{const_cast<void*>(out), query, key_cache, value_cache, block_tables,
+                 max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                 head_size, block_size, num_blocks, max_context_len, 1.f, (pa_dtype)dtype,
+                 nullptr, nullptr};
+    a.partition_size = partition_size;
+    pa_status st = check_decode(a);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % block_size)
+        return fail(PA_ERR_INVALID_ARG, "decode_v2: partition_size %d must be a positive multiple "
+                    "of block_size %d", partition_size, block_size);
+    return PA_OK;
+}
 
 int32_t set_last_error(int32_t status, const char* message) {
     g_last_error = message ? message : "";

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "pa_once.h"
+
 namespace pa {
 
 // Head of the V2 workspace.  The plan kernel writes it; the decode kernel's persistent
@@ -107,6 +109,15 @@ cudaError_t launch_copy_blocks(void* key_cache, void* value_cache, const int32_t
                                int32_t num_pairs, int64_t bytes_per_block, int32_t num_blocks,
                                int32_t* status, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+// The argument checks pa_decode_v2 makes before it looks at its workspace: PA_OK, or the
+// status it would return (with this thread's pa_last_error() message set).
+int32_t check_decode_v2_args(const void* out, const void* query, const void* key_cache,
+                             const void* value_cache, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_size, int32_t block_size, int32_t num_blocks,
+                             int32_t max_context_len, int32_t dtype, int32_t partition_size);
 
 // Records `message` as this thread's pa_last_error() text and returns `status`.
 int32_t set_last_error(int32_t status, const char* message);

@@ -56,6 +56,12 @@ extern "C" pa_status pa_decode_v2_noalloc(
     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
     int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale, pa_dtype dtype,
     int32_t partition_size, int32_t* status_dev, pa_stream stream) {
+    // the same argument checks (and errors) as pa_decode_v2, before the scratch size
+    const int32_t chk = pa::check_decode_v2_args(
+        out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+        num_seqs, num_q_heads, num_kv_heads, head_size, block_size, num_blocks, max_context_len,
+        (int32_t)dtype, partition_size);
+    if (chk != PA_OK) return (pa_status)chk;
     const size_t need = pa_decode_v2_workspace_size(num_seqs, num_q_heads, head_size,
                                                     max_context_len, partition_size);
     if (need > PA_NOALLOC_SCRATCH_BYTES) {

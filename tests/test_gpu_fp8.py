@@ -110,3 +110,34 @@ def test_fp8_copy_blocks_and_padding_slots(cuda_device):
     pa.pa_reshape_and_cache_fp8(key, key, kc, vc, slots, 0.5, 0.25)
     torch.cuda.synchronize()
     assert bool((kc[0, :, 3] == 0x40).all()) and bool((vc[0, :, 3] == 0x48).all())   # 2.0, 4.0
+
+
+@pytest.mark.parametrize("name", ["l3_8b", "l3_70b"])
+def test_fp8_full_size_every_row(cuda_device, name):
+    """A full-size batch over fp8 pools (Llama-3-8B heads with 16-token blocks, and
+    Llama-3-70B heads with 32-token blocks): the prefill and the step's rows quantised by
+    the product's scatter equal the oracle's whole pools bit for bit, and every output
+    row of the automatic choice (the device-sized V2 plan) and of V1 meets the bound."""
+    import paged_kv_cache_187_gb300 as pa
+    from paged_kv_cache_187_gb300 import workloads as W
+    from paged_kv_cache_187_gb300.runner import DecodeRunner
+    from oracle_side import OracleState, err_stats, record_step
+    w = W.WORKLOADS[name]
+    r = DecodeRunner(w, device="cuda", kv_fp8=True).next_step()
+    r.run_reshape()
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    st = record_step(r)
+    o = OracleState(r, [st])
+    assert np.array_equal(_u8(r.key_cache), o.k_cache)
+    assert np.array_equal(_u8(r.value_cache), o.v_cache)
+    del r.k_prefill, r.v_prefill
+    ref = o.decode(0, st)
+    for variant in ("auto", "v1"):
+        r.out.fill_(5.0)
+        r.run_decode(variant)
+        torch.cuda.synchronize()
+        assert int(r.status.item()) == 0
+        e = err_stats(bits(r.out), ref, w.dtype)
+        print(f"fp8 {name} {variant}: {e}")
+        assert e.ok(w.dtype), f"fp8 {name} {variant}: {e}"

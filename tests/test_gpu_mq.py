@@ -163,3 +163,39 @@ def test_multi_query_host_errors(cuda_device):
     with pytest.raises(pa.PAError):
         pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, 20, 0.1, variant="v2",
                         partition_size=32, workspace=None)
+
+
+@pytest.mark.parametrize("name,q_lens", [("l3_8b", (4,)), ("l3_70b", (2, 4))])
+def test_multi_query_full_size_every_row(cuda_device, name, q_lens):
+    """Multi-query decode over a full-size batch's pools (the last q_len tokens of every
+    context are the new ones), through the launch pa_decode_mq picks by itself: Llama-3-8B
+    heads with 4 tokens (16 rows per kv head, the tcgen05 kernel), Llama-3-70B heads with
+    2 tokens (16 rows, 32-token blocks: mma.sync) and 4 tokens (32 rows: tcgen05).  Every
+    (sequence, token, head) row against the oracle."""
+    import paged_kv_cache_187_gb300 as pa
+    from paged_kv_cache_187_gb300 import workloads as W
+    from paged_kv_cache_187_gb300.runner import DecodeRunner
+    from oracle_side import OracleState, err_stats, record_step
+    w = W.WORKLOADS[name]
+    r = DecodeRunner(w, device="cuda").next_step()
+    r.run_reshape()
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    st = record_step(r)
+    o = OracleState(r, [st])
+    del r.k_prefill, r.v_prefill
+    S, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
+    mcl = r.step_max_context_len()
+    for QL in q_lens:
+        q = W.randn_16bit((S, QL, Hq, D), w.dtype, W.stream_seed(w, "q", 1 + QL), r.device)
+        out = torch.full_like(q, 5.0)
+        need = pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, w.block_size, mcl, 0)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=r.device)
+        pa.pa_decode_mq(out, q, r.key_cache, r.value_cache, r.block_tables_d, r.context_lens_d,
+                        mcl, w.scale, workspace=ws, status=r.status)
+        torch.cuda.synchronize()
+        assert int(r.status.item()) == 0
+        ref = o.decode_mq(0, bits(q))
+        e = err_stats(bits(out), ref, w.dtype)
+        print(f"mq {name} q_len {QL}: {e}")
+        assert e.ok(w.dtype), f"mq {name} q_len {QL}: {e}"

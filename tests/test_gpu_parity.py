@@ -2,10 +2,12 @@
 
 Bars (stated by the workload specification):
   * reshape_and_cache, the allocator's slots and block tables: bit-exact;
-  * decode: max |gpu - round_to_dtype(oracle)| <= 2e-3 (fp16) and <= 1e-2 (bf16).
-Small cases compare every output; full-size workloads compare sampled (sequence, head)
-rows -- always including the shortest and longest contexts -- that the oracle
-recomputes one by one, plus properties that hold at any size.
+  * decode: max |gpu - round_to_dtype(oracle)| <= 2e-3 (fp16) and <= 1e-2 (bf16), with
+    the one-ulp allowance for outputs whose ulp exceeds that bound, and a cap on how
+    many elements may need it (oracle_side.ErrStats.ok).
+Every (sequence, head) row is compared, at full size too: the oracle's sequences are
+fanned out over the host's cores (each range runs the plain single-threaded oracle).
+The middle steps of the multi-step loop compare sampled rows.
 """
 import dataclasses
 import math
@@ -15,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from oracle_side import OracleState, StepRecord, TOL, bits, max_err, record_step
+from oracle_side import OracleState, StepRecord, TOL, bits, err_stats, max_err, record_step
 
 pytestmark = pytest.mark.gpu
 
@@ -150,25 +152,35 @@ def test_decode_step_single_call_tiny(cuda_device):
 
 
 @pytest.mark.parametrize("name", ["l2_7b", "l3_8b", "skew"])
-def test_decode_full_size_sampled(cuda_device, name):
+def test_decode_full_size_every_row(cuda_device, name):
+    """The whole batch of one full-size decode step: every output element of every
+    (sequence, head) row against the oracle, for the auto choice, V1, and V2 at the
+    workload's partition size and at 256 tokens; the whole pools bit for bit."""
     w = W.WORKLOADS[name]
     r = _runner(w).next_step()
     r.run_reshape()
+    _status_ok(r)
     st = record_step(r)
-    seqs, rows = _sample_rows(r)
-    o = OracleState(r, [st], seqs=seqs)
-    ref = o.decode(0, st, rows=rows)
+    o = OracleState(r, [st])
+    assert np.array_equal(o.step_slots[0], r.slots)
+    assert np.array_equal(o.step_tables[0], r.block_tables)
+    assert np.array_equal(bits(r.key_cache), o.k_cache)
+    assert np.array_equal(bits(r.value_cache), o.v_cache)
+    ref = o.decode(0, st)
     for variant, P in (("auto", None), ("v1", None), ("v2", w.partition_size), ("v2", 256)):
-        r.out.zero_()
+        r.out.fill_(7.0)
         r.run_decode(variant, partition_size=P)
         _status_ok(r)
-        err = max_err(bits(r.out), ref, w.dtype, rows=rows)
-        assert err <= TOL[w.dtype], f"{name} {variant} P={P}: {err}"
-        out = r.out.float()
-        assert bool(torch.isfinite(out).all())
+        e = err_stats(bits(r.out), ref, w.dtype)
+        print(f"{name} {variant} P={P}: {e}")
+        assert e.ok(w.dtype), f"{name} {variant} P={P}: {e}"
 
 
 def test_multistep_loop_l3_70b(cuda_device):
+    """Eight steps of the Llama-3-70B-shaped loop (append, reshape_and_cache, auto decode
+    per step): slots, tables and lengths bit-exact at every step; every row of the
+    first and the last step against the oracle, sampled rows of the steps between; the
+    pools bit for bit after the loop."""
     w = W.WORKLOADS["l3_70b"]
     r = _runner(w)
     recs, outs = [], []
@@ -178,17 +190,19 @@ def test_multistep_loop_l3_70b(cuda_device):
         recs.append(record_step(r))
         outs.append(bits(r.out))
     _status_ok(r)
-    seqs, rows = _sample_rows(r, n_seq=8)
-    o = OracleState(r, recs, seqs=seqs)
+    _, rows = _sample_rows(r, n_seq=8)
+    o = OracleState(r, recs)
     for k in range(w.steps):
         assert np.array_equal(o.step_slots[k], recs[k].slots)
         assert np.array_equal(o.step_tables[k], recs[k].block_tables)
         assert np.array_equal(o.step_lens[k], recs[k].context_lens)
-        ref = o.decode(k, recs[k], rows=rows)
-        err = max_err(outs[k], ref, w.dtype, rows=rows)
-        assert err <= TOL[w.dtype], f"step {k}: {err}"
-    used = torch.from_numpy(o.used_blocks).to(cuda_device)
-    assert np.array_equal(bits(r.key_cache.index_select(0, used)), o.k_cache)
+        every = k in (0, w.steps - 1)
+        ref = o.decode(k, recs[k]) if every else o.decode(k, recs[k], rows=rows)
+        e = err_stats(outs[k], ref, w.dtype, rows=None if every else rows)
+        print(f"l3_70b step {k} ({'every row' if every else 'sampled rows'}): {e}")
+        assert e.ok(w.dtype), f"step {k}: {e}"
+    assert np.array_equal(bits(r.key_cache), o.k_cache)
+    assert np.array_equal(bits(r.value_cache), o.v_cache)
 
 
 # ----------------------------------------------------------------------------- GPU pins
@@ -234,6 +248,52 @@ def test_gqa_tensor_core_and_cuda_core_paths(cuda_device):
                 assert err <= TOL[w.dtype], f"mma={mma} {variant}: {err}"
     finally:
         pa.pa_set_gqa_tensor_cores(True)
+
+
+def test_kernel_choice_belongs_to_the_calling_thread(cuda_device):
+    """pa_set_gqa_tensor_cores(0) in one thread leaves another thread's calls on the
+    tensor-core path: the main thread's output stays bit-identical to its own earlier
+    tensor-core result while the other thread's setting is off."""
+    import threading
+    pa = _pa()
+    w = dataclasses.replace(W.WORKLOADS["l3_8b"], num_seqs=8)
+    lens = np.array([3, 40, 200, 513, 999, 1500, 64, 17], np.int32)
+    r = _runner(w, start_lens=lens).next_step()
+    r.run_reshape()
+    r.run_decode("v1")
+    _status_ok(r)
+    mma = bits(r.out)
+    done = threading.Event()
+    release = threading.Event()
+
+    def other():
+        pa.pa_set_gqa_tensor_cores(False)
+        done.set()
+        release.wait(30)
+
+    t = threading.Thread(target=other)
+    t.start()
+    assert done.wait(30)
+    try:
+        r.out.zero_()
+        r.run_decode("v1")
+        _status_ok(r)
+        assert np.array_equal(bits(r.out), mma)
+    finally:
+        release.set()
+        t.join()
+    # in the main thread the same switch does take effect (both paths meet the bound)
+    st = record_step(r)
+    ref = OracleState(r, [st]).decode(0, st)
+    try:
+        pa.pa_set_gqa_tensor_cores(False)
+        r.run_decode("v1")
+        _status_ok(r)
+        core = bits(r.out)
+    finally:
+        pa.pa_set_gqa_tensor_cores(True)
+    assert max_err(core, ref, w.dtype) <= TOL[w.dtype]
+    assert max_err(mma, ref, w.dtype) <= TOL[w.dtype]
 
 
 EDGE = []

@@ -119,3 +119,87 @@ def test_decode_mq_checks(lib, q_len, Hkv, variant, code, word):
     assert lib.pa_decode_mq(A, A, A, A, A, 4, A, 2, q_len, 8, Hkv, 128, 16, 64, 64, 0.1, BF16,
                             variant, 0, A, 1 << 30, None, None) == code
     assert word in _err(lib)
+
+
+def _noalloc(lib, P=64, **kw):
+    p = dict(out=A, q=A, kc=A, vc=A, bt=A, maxb=4, lens=A, S=2, Hq=8, Hkv=2, D=128, bs=16,
+             NB=64, mcl=64, scale=0.1, dt=BF16)
+    p.update(kw)
+    return lib.pa_decode_v2_noalloc(p["out"], p["q"], p["kc"], p["vc"], p["bt"], p["maxb"],
+                                    p["lens"], p["S"], p["Hq"], p["Hkv"], p["D"], p["bs"], p["NB"],
+                                    p["mcl"], p["scale"], p["dt"], P, None, None)
+
+
+def test_noalloc_checks_arguments_before_its_scratch_size(lib):
+    huge = 1 << 22
+    # valid arguments whose partials exceed the fixed scratch: PA_ERR_WORKSPACE, no launch
+    assert _noalloc(lib, P=16, S=64, Hq=32, Hkv=8, mcl=huge, maxb=huge // 16) == WORKSPACE
+    assert "scratch" in _err(lib)
+    # the same sizes with a bad argument report that argument, as pa_decode_v2 does
+    assert _noalloc(lib, P=16, S=64, Hq=32, Hkv=8, D=96, mcl=huge, maxb=huge // 16) == UNSUPPORTED
+    assert _v2(lib, P=16, S=64, Hq=32, Hkv=8, D=96, mcl=huge, maxb=huge // 16) == UNSUPPORTED
+    assert _noalloc(lib, P=24, mcl=huge, maxb=huge // 16) == INVALID
+    assert "partition_size" in _err(lib)
+    assert _noalloc(lib, out=MIS) == INVALID
+
+
+def test_noalloc_scratch_size_agrees_between_header_and_binding():
+    import os
+    import re
+    import paged_kv_cache_187_gb300 as pa
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "pa.h")).read()
+    m = re.search(r"#define\s+PA_NOALLOC_SCRATCH_BYTES\s+(.+)", text)
+    expr = m.group(1).replace("(size_t)", "")
+    assert pa.PA_NOALLOC_SCRATCH_BYTES == eval(expr, {}) == 64 << 20
+
+
+def test_per_device_set_up_runs_once_per_device_ordinal(tmp_path):
+    """The launchers' shared-memory attribute bookkeeping (pa_once.h), compiled into a
+    host-only program: set-up runs once on each of two device ordinals, a failed attempt
+    is retried, and eight threads racing on both ordinals still run it once per device."""
+    import os
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    if not gxx:
+        pytest.skip("g++ not found")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "once.cpp"
+    src.write_text(r'''
+#include <atomic>
+#include <cstdio>
+#include <thread>
+#include <vector>
+#include "pa_once.h"
+int main() {
+    pa::PerDeviceOnce once;
+    int calls[3] = {0, 0, 0};
+    auto set_up = [&](int dev) { return once.run(dev, [&] { ++calls[dev]; return 0; }); };
+    if (set_up(0) || set_up(0) || set_up(1) || set_up(1) || set_up(0)) return 1;
+    if (calls[0] != 1 || calls[1] != 1 || !once.done(0) || !once.done(1) || once.done(2)) return 2;
+    // a failing set-up (e.g. an attribute the device refused) is tried again
+    int tries = 0;
+    if (once.run(2, [&] { ++tries; return 7; }) != 7 || once.done(2)) return 3;
+    if (once.run(2, [&] { ++tries; return 0; }) != 0 || !once.done(2) || tries != 2) return 4;
+    // concurrent first calls on two devices
+    pa::PerDeviceOnce shared;
+    std::atomic<int> per_dev[2];
+    per_dev[0] = 0; per_dev[1] = 0;
+    std::vector<std::thread> ts;
+    for (int t = 0; t < 8; ++t)
+        ts.emplace_back([&, t] {
+            for (int i = 0; i < 1000; ++i) shared.run((t + i) % 2, [&] { ++per_dev[(t + i) % 2]; return 0; });
+        });
+    for (auto& th : ts) th.join();
+    if (per_dev[0] != 1 || per_dev[1] != 1) return 5;
+    std::puts("ok");
+    return 0;
+}
+''')
+    exe = tmp_path / "once"
+    subprocess.run([gxx, "-std=c++17", "-O1", "-pthread", "-I",
+                    os.path.join(root, "paged_kv_cache_187_gb300", "csrc"), str(src), "-o", str(exe)],
+                   check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
