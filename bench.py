@@ -114,7 +114,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -747,8 +747,14 @@ def run_profile_case(args):
     import paged_kv_cache_187_gb300 as pa
     from paged_kv_cache_187_gb300 import workloads as W
     from paged_kv_cache_187_gb300.runner import DecodeRunner
+    import dataclasses
     w = W.WORKLOADS[args.profile_workload]
-    r = DecodeRunner(w, device="cuda", kv_fp8=args.kv_fp8).next_step()
+    start_lens = None
+    if args.num_seqs:
+        # the first num_seqs sequences of the workload, with their own context lengths
+        start_lens = W.start_context_lens(w)[:args.num_seqs]
+        w = dataclasses.replace(w, num_seqs=args.num_seqs)
+    r = DecodeRunner(w, device="cuda", kv_fp8=args.kv_fp8, start_lens=start_lens).next_step()
     r.run_reshape()
     del r.k_prefill, r.v_prefill          # not needed for decoding: keep the footprint small
     torch.cuda.empty_cache()
@@ -778,7 +784,8 @@ def run_profile_case(args):
         decode()
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0
-    print(json.dumps({"profile_case": w.name, "kv_fp8": bool(args.kv_fp8), "variant": variant,
+    print(json.dumps({"profile_case": w.name, "num_seqs": w.num_seqs,
+                      "context_tokens": r.seq_tokens(), "kv_fp8": bool(args.kv_fp8), "variant": variant,
                       "q_len": args.q_len, "steps": args.steps,
                       "warmup": args.warmup, "gqa_cuda_cores": bool(args.gqa_cuda_cores),
                       # K/V once, plus q_len query and output rows per (sequence, head)
@@ -807,6 +814,8 @@ def main():
                     help="profile case: force the CUDA-core path for grouped-query heads")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="profile case: keep the KV pools in fp8 E4M3")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="profile case: only the first N sequences of the workload")
     ap.add_argument("--q-len", type=int, default=1,
                     help="profile case: multi-query decode with this many query tokens per sequence")
     ap.add_argument("--multistep", type=int, default=0,

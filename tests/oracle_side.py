@@ -208,7 +208,7 @@ class ErrStats:
     n_ulp: int        # elements beyond the stated bound, admitted only as one ulp
     max_abs: float    # max |gpu - round(oracle)| over all compared elements
 
-    def ok(self, dtype: str, max_ulp_frac: float = 1e-4) -> bool:
+    def ok(self, dtype: str, max_ulp_frac: float = 1e-5) -> bool:
         """The gate, plus a bound on how often the one-ulp allowance was needed."""
         return self.err <= TOL[dtype] and self.n_ulp <= max(2, max_ulp_frac * self.n)
 
