@@ -244,10 +244,9 @@ pa_status pa_decode_mq(void* out, const void* query, const void* key_cache, cons
                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
                        pa_stream stream);
 
-/* Selects the multi-query kernel for head_size 128 with 16-bit caches and more than 16
- * query rows (q_len x group) per kv head, or more than 8 with 16-token blocks: 1 (the
- * default) runs it on the 5th-generation tensor cores (tcgen05, accumulators in tensor
- * memory), 0 on mma.sync.  Other shapes, and fixed V2 partition sizes that are not a
+/* Selects the multi-query kernel for head_size 128 with 16-bit caches and more than 8
+ * query rows (q_len x group) per kv head: 1 (the default) runs it on the 5th-generation
+ * tensor cores (tcgen05, accumulators in tensor memory), 0 on mma.sync.  Other shapes, and fixed V2 partition sizes that are not a
  * multiple of 128 tokens, always take the mma.sync kernel.  The setting belongs to the
  * calling thread: it changes that thread's later calls only (each thread starts at 1).
  * Returns PA_OK. */

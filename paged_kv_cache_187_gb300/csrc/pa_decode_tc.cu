@@ -1,5 +1,5 @@
 // Multi-query decode kernels on tcgen05 (head_size 128): fp16 / bf16, 16- or 32-token
-// blocks, 16 (16-token blocks only) or 32 query rows per unit.
+// blocks, 16 or 32 query rows per unit.
 #include "pa_decode_tc.cuh"
 
 namespace pa {
@@ -49,13 +49,13 @@ cudaError_t launch_decode_mq_tc(const KernelKey& k, const CUtensorMap& kmap, con
 #define PA_CASE(BF16_, BS_, R_)                                                              \
     if (k.bf16 == BF16_ && k.block_size == BS_ && k.heads_cap == R_)                         \
         return launch_tc<BF16_, BS_, R_>(kmap, vmap, p, persistent, num_units, stream, occ);
-    // 16-row units only with 16-token blocks: with 32-token blocks the dispatch keeps up to
-    // 16 rows on the mma.sync kernel
     PA_CASE(true, 16, 16)
     PA_CASE(true, 16, 32)
+    PA_CASE(true, 32, 16)
     PA_CASE(true, 32, 32)
     PA_CASE(false, 16, 16)
     PA_CASE(false, 16, 32)
+    PA_CASE(false, 32, 16)
     PA_CASE(false, 32, 32)
 #undef PA_CASE
     return cudaErrorInvalidValue;

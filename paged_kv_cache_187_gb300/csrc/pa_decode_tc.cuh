@@ -75,6 +75,7 @@ struct alignas(1024) TcSmem {
     uint8_t p[2][2 * C::PHALF];              // P^T of two consecutive tiles
     alignas(16) float red[2][C::RPAD][4];   // per-warp column maxima, by tile parity
     alignas(16) float lred[C::RPAD][4];     // per-warp column exp-sums (epilogue)
+    alignas(16) uint16_t ostage[C::RPAD][kD];   // a unit's output rows on their way out
     uint64_t k_full[C::NK], k_empty[C::NK], v_full[C::NV], v_empty[C::NV];
     uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t q_full[2], q_empty[2], o_full, o_empty, drain;
@@ -659,20 +660,43 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 break;
             }
             const bool final_out = u.pslot < 0;
+            // Row n's exp-sum in lane n (< RPAD) of every warp: the per-row values are
+            // computed once, in parallel, and handed to the other lanes by shuffles.
+            float L_row = 0.f;
+            if (lane < RPAD) {
+                const float4 l4 = *reinterpret_cast<const float4*>(sm.lred[lane]);
+                L_row = (l4.x + l4.y) + (l4.z + l4.w);
+            }
+            if (final_out) {
+                // the unit's rows, normalised and rounded, staged [row][dim] in shared
+                // memory; then written out in 16-byte pieces (a row is 256 contiguous bytes)
+                const float inv_row = L_row > 0.f ? p.out_scale / L_row : 0.f;
 #pragma unroll
-            for (int n = 0; n < RPAD; ++n) {
-                const float4 l4 = *reinterpret_cast<const float4*>(sm.lred[n]);
-                const float L = (l4.x + l4.y) + (l4.z + l4.w);
-                if (n < u.nrows) {
-                    if (final_out) {
-                        const float inv = L > 0.f ? p.out_scale / L : 0.f;
-                        reinterpret_cast<uint16_t*>(p.out)[mq_out_row(p, u.seq, u.kvh, u.row0 + n) * kD + row] =
-                            to16<C::kBf16>(o[n] * inv);
-                    } else {
-                        const size_t pr = part_row(p, u, u.pslot, n);
-                        p.part_acc[pr * kD + row] = o[n];
-                        if (tid == 0) p.part_ml[pr] = make_float2(m[n], L);
+                for (int n = 0; n < RPAD; ++n)
+                    sm.ostage[n][row] = to16<C::kBf16>(o[n] * __shfl_sync(0xffffffffu, inv_row, n));
+                named_bar_sync(kBarSoft, kSoftThreads);
+                constexpr int kPieces = RPAD * kD * 2 / 16;
+#pragma unroll
+                for (int k = 0; k < kPieces / kSoftThreads; ++k) {
+                    const int c = tid + kSoftThreads * k, n = c >> 4, piece = c & 15;
+                    if (n < u.nrows) {
+                        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) +
+                                        mq_out_row(p, u.seq, u.kvh, u.row0 + n) * kD + piece * 8;
+                        *reinterpret_cast<uint4*>(dst) =
+                            *reinterpret_cast<const uint4*>(&sm.ostage[n][piece * 8]);
                     }
+                }
+            } else {
+                // unnormalised partial rows of this partition, and (m, l) of each row
+                const size_t pr0 = part_row(p, u, u.pslot, 0);
+#pragma unroll
+                for (int n = 0; n < RPAD; ++n)
+                    if (n < u.nrows) p.part_acc[(pr0 + n) * kD + row] = o[n];
+                if (sw == 0 && lane < u.nrows) {
+                    float mr = 0.f;
+#pragma unroll
+                    for (int n = 0; n < RPAD; ++n) mr = n == lane ? m[n] : mr;
+                    p.part_ml[pr0 + lane] = make_float2(mr, L_row);
                 }
             }
             if (!final_out) {

@@ -194,17 +194,23 @@ struct DecodeArgs {
 // The tcgen05 multi-query kernel takes head_size 128, 16-bit caches, and partitions that
 // are multiples of its 128-token tile; it holds 16 or 32 query rows per unit.  It is used
 // where it measured faster than the mma.sync kernel, whose three CTAs per SM hide the load
-// latency better than its single tile pipeline per SM: above 16 query rows per kv head,
-// and above 8 with 16-token blocks (Llama-3-8B / -70B batches: 8 rows 231 vs 197 us;
-// 16 rows 244 vs 266 us with 16-token blocks, 690 vs 647 us with 32-token blocks; 32 rows
-// 357 vs 366 us and 928 vs 1034 us).
+// latency better than its single tile pipeline per SM: above 8 query rows per kv head
+// (Llama-3-8B / -70B batches, decode kernel: 8 rows with 16-token blocks 210 vs 205 us;
+// 16 rows 212 vs 269 us with 16-token blocks, 635 vs 666 us with 32-token blocks; 32 rows
+// 263 vs 395 us and 748 vs 1084 us).
+#ifndef PA_MQ_TC_ROWS_BS32
+#define PA_MQ_TC_ROWS_BS32 8    // tcgen05 above this many rows per kv head, 32-token blocks
+#endif
+#ifndef PA_MQ_TC_ROWS_BS16
+#define PA_MQ_TC_ROWS_BS16 8    // ... and with 16-token blocks
+#endif
 bool use_mq_tc(const DecodeArgs& a) {
     const int32_t rows = a.q_len * (a.num_q_heads / std::max(a.num_kv_heads, 1));
-    const bool wins = rows > 16 || (rows > 8 && a.block_size == 16);
+    const bool wins = a.block_size == 16 ? rows > PA_MQ_TC_ROWS_BS16 : rows > PA_MQ_TC_ROWS_BS32;
     return g_mq_tc && a.q_len > 1 && wins && a.head_size == 128 && !a.kv8 &&
            (a.partition_size == 0 || a.partition_size % pa::kTcTileTokens == 0);
 }
-// Rows per unit of the tcgen05 kernel (16-row units exist for 16-token blocks only).
+// Rows per unit of the tcgen05 kernel: 16 or 32.
 // fp8 caches with 16-token blocks are decoded in tiles of two blocks (32 tokens), which
 // needs partitions that are multiples of 32 tokens.
 int32_t tile_blocks_for(const DecodeArgs& a) {
@@ -215,9 +221,7 @@ int32_t tile_blocks_for(const DecodeArgs& a) {
             (a.partition_size == 0 || a.partition_size % 32 == 0)) ? 2 : 1;
 }
 
-int32_t mq_tc_rows(int32_t rows, int32_t block_size) {
-    return rows <= 16 && block_size == 16 ? 16 : 32;
-}
+int32_t mq_tc_rows(int32_t rows, int32_t) { return rows <= 16 ? 16 : 32; }
 
 // Multi-query kernels: rows per consumer (the head capacity), consumer warps per CTA, row
 // groups per unit (a power of two dividing the consumers, so that the consumers of a

@@ -58,9 +58,9 @@ def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
 
 
 # (dtype, q_len, Hq, Hkv, D, bs): rows per (sequence, kv head) = q_len * group.  With
-# head_size 128 the tcgen05 kernel takes cases above 16 rows, or above 8 with 16-token
-# blocks (16 or 32 rows per unit), unless the test switches it off; otherwise the mma.sync
-# kernel (up to 4 row groups of 8 rows per unit).
+# head_size 128 the tcgen05 kernel takes cases above 8 rows (16 or 32 rows per unit),
+# unless the test switches it off; otherwise the mma.sync kernel (up to 4 row groups of 8
+# rows per unit).
 CASES = [
     ("bf16", 4, 32, 8, 128, 16),   # 16 rows: one 16-row unit (Llama-3-8B heads)
     ("f16", 2, 32, 8, 128, 32),    # 8 rows, 32-token blocks
@@ -169,8 +169,8 @@ def test_multi_query_host_errors(cuda_device):
 def test_multi_query_full_size_every_row(cuda_device, name, q_lens):
     """Multi-query decode over a full-size batch's pools (the last q_len tokens of every
     context are the new ones), through the launch pa_decode_mq picks by itself: Llama-3-8B
-    heads with 4 tokens (16 rows per kv head, the tcgen05 kernel), Llama-3-70B heads with
-    2 tokens (16 rows, 32-token blocks: mma.sync) and 4 tokens (32 rows: tcgen05).  Every
+    heads with 4 tokens (16 rows per kv head), Llama-3-70B heads with 2 tokens (16 rows,
+    32-token blocks) and 4 tokens (32 rows), all on the tcgen05 kernel.  Every
     (sequence, token, head) row against the oracle."""
     import paged_kv_cache_187_gb300 as pa
     from paged_kv_cache_187_gb300 import workloads as W
