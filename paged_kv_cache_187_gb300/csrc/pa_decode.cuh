@@ -704,6 +704,13 @@ struct MmaConsumer {
                 lt[nt][j] = v;
             }
         const bool final_out = u.pslot < 0;
+        // one reciprocal per column (query row) this lane holds, not one per element
+        float inv[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                inv[nt][j] = !final_out ? 1.f : lt[nt][j] > 0.f ? p.out_scale / lt[nt][j] : 0.f;
         // stage [head][dim] in fp32 so the rows leave as contiguous vectors
 #pragma unroll
         for (int i = 0; i < KS; ++i)
@@ -713,12 +720,7 @@ struct MmaConsumer {
                 for (int r = 0; r < 4; ++r) {
                     const int d = out_dim(i, lane, r);
                     const int h = nt * 8 + 2 * (lane & 3) + (r & 1);
-                    float v = acc[i][nt][r];
-                    if (final_out) {
-                        const float den = lt[nt][r & 1];
-                        v = den > 0.f ? v * p.out_scale / den : 0.f;
-                    }
-                    ostage[h * D + d] = v;
+                    ostage[h * D + d] = acc[i][nt][r] * inv[nt][r & 1];
                 }
         __syncwarp();
         const int nr = u.nrows;
