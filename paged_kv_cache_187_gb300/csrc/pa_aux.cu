@@ -37,7 +37,12 @@ __global__ void __launch_bounds__(128)
                              const int32_t* __restrict__ slot_mapping, int32_t num_kv_heads,
                              int32_t head_size, int32_t block_size, int32_t num_blocks,
                              int32_t* status) {
-    allow_dependent_launch();   // the decode kernel may set up meanwhile (it waits for us)
+    // The kernel after this one (a decode, or a plan) may launch meanwhile: a decode waits
+    // for this kernel before it reads the pools, a plan reads only the context lengths.
+    // Nothing is read or written here before the kernel before this one has finished: a
+    // decode may still be reading blocks that this step's slots reuse.
+    allow_dependent_launch();
+    grid_dependency_wait();
     const int32_t i = blockIdx.x;
     const int64_t slot = slot_mapping[i];
     if (slot < 0) return;                                   // padding token
@@ -70,7 +75,8 @@ __global__ void __launch_bounds__(128)
                                  const int32_t* __restrict__ slot_mapping, int32_t num_kv_heads,
                                  int32_t head_size, int32_t block_size, int32_t num_blocks,
                                  float k_inv, float v_inv, int32_t* status) {
-    allow_dependent_launch();
+    allow_dependent_launch();   // as in reshape_and_cache_kernel
+    grid_dependency_wait();
     const int32_t i = blockIdx.x;
     const int64_t slot = slot_mapping[i];
     if (slot < 0) return;
@@ -260,9 +266,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         p.hdr->partition_size = (uint32_t)P;
         p.hdr->counter = 0;
     }
-    // This kernel may run alongside the reshape_and_cache launch before it (it reads
-    // nothing that launch writes).  Finish only after that launch has, so that the
-    // decode kernel, which waits for this one, also sees the new K/V rows.
+    // This kernel may start before the kernel ahead of it on the stream has finished (a
+    // decode running its last units, or a reshape_and_cache): it reads only the context
+    // lengths and writes only this call's half of the workspace.  It finishes only after
+    // that kernel has, so that whatever waits for this one finds everything before done.
     grid_dependency_wait();
 }
 
@@ -333,6 +340,25 @@ __global__ void __launch_bounds__(32) wait_timeout_probe_kernel(int32_t* status,
     if (threadIdx.x == 0 && !ok && status) atomicOr(status, 8 /* PA_DEVERR_TIMEOUT */);
 }
 
+// Launches `kern` as a programmatic dependent of the kernel before it on `stream`: it may
+// start while that kernel still runs and waits for it (griddepcontrol.wait) before it
+// touches memory.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(dim3 grid, dim3 block, cudaStream_t stream, void (*kern)(KArgs...),
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
 
 cudaError_t launch_advance_step(int32_t* context_lens, int32_t* slot_mapping,
@@ -341,6 +367,8 @@ cudaError_t launch_advance_step(int32_t* context_lens, int32_t* slot_mapping,
                                 int64_t* input_positions, int64_t* input_tokens,
                                 const int64_t* sampled_token_ids, int32_t* status,
                                 cudaStream_t stream) {
+    // An ordinary launch: it rewrites the lengths, which the plan kernel after it reads
+    // before it waits for its predecessor, so it must have finished when that one starts.
     const int32_t threads = 256;
     advance_step_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
         context_lens, slot_mapping, block_tables, max_blocks_per_seq, num_seqs, block_size,
@@ -371,11 +399,10 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                                      int32_t head_size, int32_t block_size, int32_t num_blocks,
                                      int32_t* status, cudaStream_t stream) {
     if (num_tokens <= 0) return cudaSuccess;
-    reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-        static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), slot_mapping,
-        num_kv_heads, head_size, block_size, num_blocks, status);
-    return cudaGetLastError();
+    return launch_pdl(dim3((unsigned)num_tokens), dim3(128), stream, reshape_and_cache_kernel,
+                      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                      static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache),
+                      slot_mapping, num_kv_heads, head_size, block_size, num_blocks, status);
 }
 
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
@@ -386,17 +413,18 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, voi
                                          int32_t* status, cudaStream_t stream) {
     if (num_tokens <= 0) return cudaSuccess;
     auto kern = src_bf16 ? reshape_and_cache_fp8_kernel<true> : reshape_and_cache_fp8_kernel<false>;
-    kern<<<num_tokens, 128, 0, stream>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-        static_cast<uint2*>(key_cache), static_cast<uint2*>(value_cache), slot_mapping,
-        num_kv_heads, head_size, block_size, num_blocks, k_inv_scale, v_inv_scale, status);
-    return cudaGetLastError();
+    return launch_pdl(dim3((unsigned)num_tokens), dim3(128), stream, kern,
+                      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                      static_cast<uint2*>(key_cache), static_cast<uint2*>(value_cache),
+                      slot_mapping, num_kv_heads, head_size, block_size, num_blocks, k_inv_scale,
+                      v_inv_scale, status);
 }
 
 cudaError_t launch_plan(const DecodeParams& p, cudaStream_t stream) {
-    // Programmatic dependent launch: may start while a preceding reshape_and_cache runs.
-    // A preceding decode kernel never lets it start early, so the workspace it rewrites
-    // is no longer in use when it does.
+    // Programmatic dependent launch: may start while a preceding reshape_and_cache or
+    // decode kernel still runs.  It rewrites only the half of the workspace that this call
+    // uses, which the decode of the call before on this workspace does not (halves
+    // alternate), and reads only the context lengths, final before the call.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
     // one thread per sequence, between kTailBuckets (the bucket scan takes one thread per

@@ -1127,7 +1127,17 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_CTAS)
                 }
                 break;
             }
-            if (u.seq < 0) break;
+            if (u.seq < 0) {
+                // Every tile of this CTA is issued.  Once all CTAs are here, the kernels
+                // queued after this one (the next call's plan / reshape / decode, each waiting
+                // for this kernel before it touches what this one uses) may launch: their
+                // launch and the plan's work overlap the last tiles.  (Letting them launch
+                // when a CTA starts its last unit measured slower: CTAs of the next decode
+                // then became resident on the SMs that freed first, several of the largest
+                // units on one SM.)
+                if (PA_DECODE_TRIGGER && lane == 0) allow_dependent_launch();
+                break;
+            }
             // The next unit is claimed once at most kClaimLead of this unit's tiles are left
             // to issue: early enough that its claim, list entry and first block-table
             // entries arrive before they are needed, late enough that a CTA does not sit on

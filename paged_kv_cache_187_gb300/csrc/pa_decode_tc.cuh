@@ -282,6 +282,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            // every K tile of this CTA is issued: the kernels queued after this one may
+            // launch once all CTAs are here (each waits for this kernel before it touches
+            // what this one uses)
+            if (ok && u.seq < 0 && PA_DECODE_TRIGGER && lane == 0) allow_dependent_launch();
             if (!ok || u.seq < 0) break;
             // Q rows of the unit, staged into its Q buffer (unit parity) in the 128B-swizzled
             // K-major layout, rows past the unit's zero: loads now, stores after the first

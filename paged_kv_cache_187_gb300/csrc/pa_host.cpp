@@ -343,24 +343,80 @@ pa_status make_maps(const DecodeArgs& a, CUtensorMap* km, CUtensorMap* vm) {
     return encode_pool_map(vm, a.value_cache, rows, a.head_size, a.block_size, a.kv8);
 }
 
-pa_status run_v1(const DecodeArgs& a) {
+// The reshape_and_cache of a decode step (pa_decode_step), launched by the decode call
+// right before its decode kernel -- after the plan kernel, whose work then overlaps the end
+// of the decode kernel before it.
+struct StepReshape {
+    const void* key;
+    const void* value;
+    void* key_cache;
+    void* value_cache;
+    const int32_t* slot_mapping;
+    int32_t num_tokens, num_kv_heads, head_size, block_size, num_blocks;
+    int32_t* status;
+};
+
+pa_status check_reshape(const void* key, const void* value, void* key_cache, void* value_cache,
+                        const int32_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                        int32_t head_size, int32_t block_size, int32_t num_blocks, pa_dtype dtype) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: sizes must be positive");
+    if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: dtype");
+    if (head_size % 8)
+        return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: head_size must be a multiple of 8");
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: buffers must be 16-byte aligned");
+    return PA_OK;
+}
+
+cudaError_t launch_step_reshape(const StepReshape* rs, cudaStream_t st) {
+    if (!rs || rs->num_tokens <= 0) return cudaSuccess;
+    return pa::launch_reshape_and_cache(rs->key, rs->value, rs->key_cache, rs->value_cache,
+                                        rs->slot_mapping, rs->num_tokens, rs->num_kv_heads,
+                                        rs->head_size, rs->block_size, rs->num_blocks, rs->status,
+                                        st);
+}
+
+pa_status run_v1(const DecodeArgs& a, const StepReshape* rs = nullptr) {
     pa_status st = check_decode(a);
-    if (st != PA_OK || a.num_seqs == 0) return st == PA_OK ? ok() : st;
+    if (st != PA_OK) return st;
+    if (a.num_seqs == 0) {
+        cudaError_t e = launch_step_reshape(rs, a.stream);
+        return e == cudaSuccess ? ok() : cuda_fail(e, "reshape_and_cache launch");
+    }
     CUtensorMap km, vm;
     if ((st = make_maps(a, &km, &vm)) != PA_OK) return st;
     pa::DecodeParams p = base_params(a);
     p.partition_size = 0;
     const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * p.row_chunks;
     if (units > INT32_MAX) return fail(PA_ERR_UNSUPPORTED, "decode_v1: too many (seq, head) units");
-    cudaError_t e = timed_decode(kernel_key(a), km, vm, p, false, (int32_t)units, a.stream);
+    cudaError_t e = launch_step_reshape(rs, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+    e = timed_decode(kernel_key(a), km, vm, p, false, (int32_t)units, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_v1 launch");
     return ok();
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Which half of a V2 workspace the next call on it uses: the halves alternate per
+// workspace, so that two consecutive calls on one stream never share one.
+std::mutex g_half_mu;
+std::unordered_map<const void*, uint32_t> g_half;
+
+uint32_t next_half(const void* ws) {
+    std::lock_guard<std::mutex> lk(g_half_mu);
+    uint32_t& h = g_half[ws];
+    const uint32_t mine = h;
+    h ^= 1u;
+    return mine;
+}
+
 pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_t ws_bytes,
-                 bool adaptive = false) {
+                 bool adaptive = false, const StepReshape* rs = nullptr) {
     DecodeArgs a = a_in;
     a.partition_size = adaptive ? 0 : partition_size;
     pa_status st = check_decode(a);
@@ -368,7 +424,10 @@ pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_
     if (partition_size <= 0 || partition_size % a.block_size)
         return fail(PA_ERR_INVALID_ARG, "decode_v2: partition_size %d must be a positive multiple "
                     "of block_size %d", partition_size, a.block_size);
-    if (a.num_seqs == 0) return ok();
+    if (a.num_seqs == 0) {
+        cudaError_t e = launch_step_reshape(rs, a.stream);
+        return e == cudaSuccess ? ok() : cuda_fail(e, "reshape_and_cache launch");
+    }
     // partial rows per partition: q_len * num_q_heads
     const pa::WorkspaceLayout L = pa::v2_workspace_layout(a.num_seqs, a.num_q_heads * a.q_len,
                                                           a.head_size, a.max_context_len,
@@ -385,7 +444,7 @@ pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_
     pa::DecodeParams p = base_params(a);
     p.partition_size = partition_size;
     p.adaptive = adaptive ? 1 : 0;
-    uint8_t* w = static_cast<uint8_t*>(ws);
+    uint8_t* w = static_cast<uint8_t*>(ws) + next_half(ws) * L.half;
     p.hdr = reinterpret_cast<pa::WsHeader*>(w + L.hdr);
     p.part_list = reinterpret_cast<int4*>(w + L.part_list);
     p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
@@ -402,6 +461,8 @@ pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_
     p.grid_ctas = grid;
     cudaError_t e = pa::launch_plan(p, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_v2 plan launch");
+    e = launch_step_reshape(rs, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
     e = timed_decode(k, km, vm, p, true, grid, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode_v2 launch");
     return ok();
@@ -473,7 +534,8 @@ WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32
     off = align256(off + sizeof(float2) * (size_t)parts * (size_t)num_q_heads);
     L.part_acc = off;
     off = align256(off + sizeof(float) * (size_t)parts * (size_t)num_q_heads * (size_t)head_size);
-    L.total = off;
+    L.half = off;
+    L.total = 2 * off;
     return L;
 }
 
@@ -709,16 +771,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* key_cac
                                int32_t num_kv_heads, int32_t head_size, int32_t block_size,
                                int32_t num_blocks, pa_dtype dtype, int32_t* status_dev,
                                pa_stream stream) {
-    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
-        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: sizes must be positive");
-    if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: dtype");
-    if (head_size % 8)
-        return fail(PA_ERR_UNSUPPORTED, "reshape_and_cache: head_size must be a multiple of 8");
-    if (num_tokens == 0) return ok();
-    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
-        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
-    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
-        return fail(PA_ERR_INVALID_ARG, "reshape_and_cache: buffers must be 16-byte aligned");
+    pa_status st = check_reshape(key, value, key_cache, value_cache, slot_mapping, num_tokens,
+                                 num_kv_heads, head_size, block_size, num_blocks, dtype);
+    if (st != PA_OK || num_tokens == 0) return st == PA_OK ? ok() : st;
     cudaError_t e = pa::launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
                                                  num_tokens, num_kv_heads, head_size, block_size,
                                                  num_blocks, status_dev, (cudaStream_t)stream);
@@ -904,14 +959,22 @@ pa_status pa_decode_step(void* out, const void* query, const void* key, const vo
                          int32_t num_blocks, int32_t max_context_len, float scale, pa_dtype dtype,
                          void* workspace, size_t workspace_bytes, int32_t* status_dev,
                          pa_stream stream) {
-    pa_status st = pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, num_seqs,
-                                        num_kv_heads, head_size, block_size, num_blocks, dtype,
-                                        status_dev, stream);
+    // every argument is checked before anything is launched; the V2 plan goes first so
+    // that it may overlap the end of the decode before it (see launch_plan)
+    pa_status st = check_reshape(key, value, key_cache, value_cache, slot_mapping, num_seqs,
+                                 num_kv_heads, head_size, block_size, num_blocks, dtype);
     if (st != PA_OK) return st;
-    return pa_decode_auto(out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                          context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
-                          num_blocks, max_context_len, scale, dtype, workspace, workspace_bytes,
-                          status_dev, stream);
+    int32_t v = 0, P = 0;
+    st = pa_decode_auto_plan(num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                             max_context_len, &v, &P);
+    if (st != PA_OK) return st;
+    DecodeArgs a{out, query, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_size, block_size,
+                 num_blocks, max_context_len, scale, dtype, status_dev, (cudaStream_t)stream};
+    const StepReshape rs{key, value, key_cache, value_cache, slot_mapping, num_seqs, num_kv_heads,
+                         head_size, block_size, num_blocks, status_dev};
+    if (v == 1) return run_v1(a, &rs);
+    return run_v2(a, P, workspace, workspace_bytes, /*adaptive=*/true, &rs);
 }
 
 }  // extern "C"

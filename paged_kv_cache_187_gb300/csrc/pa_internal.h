@@ -63,11 +63,21 @@ struct DecodeParams {
 // warps (2 CTAs per SM) form up to 4 row groups, so a unit covers up to 32 rows in one
 // K/V pass.
 constexpr int32_t kMqRowsPerConsumer = 8;
+
+// Decode kernels let the kernels queued after them launch once every CTA has issued the
+// copies of its last tile (1), or only when they finish (0).
+#ifndef PA_DECODE_TRIGGER
+#define PA_DECODE_TRIGGER 1
+#endif
 constexpr int32_t kMqConsumersNarrow = 2;
 constexpr int32_t kMqConsumersWide = 4;
 
+// A V2 workspace holds two halves of this layout (offsets within a half; `half` is the
+// stride between them).  Consecutive decode calls on one workspace use alternate halves,
+// so that a call's plan kernel may run while the decode kernel of the call before still
+// finishes its last units.
 struct WorkspaceLayout {
-    size_t hdr, part_list, arrive, part_ml, part_acc, total;
+    size_t hdr, part_list, arrive, part_ml, part_acc, half, total;
 };
 
 WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
