@@ -444,7 +444,11 @@ pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_
     pa::DecodeParams p = base_params(a);
     p.partition_size = partition_size;
     p.adaptive = adaptive ? 1 : 0;
-    uint8_t* w = static_cast<uint8_t*>(ws) + next_half(ws) * L.half;
+    // The first half starts at the workspace's start, the second ends at its end: two
+    // consecutive calls with different sizes then never overlap (each call's workspace
+    // holds two of its own halves, so the two halves of any two calls fit side by side).
+    const size_t top = (ws_bytes & ~size_t(255)) - L.half;
+    uint8_t* w = static_cast<uint8_t*>(ws) + (next_half(ws) ? top : 0);
     p.hdr = reinterpret_cast<pa::WsHeader*>(w + L.hdr);
     p.part_list = reinterpret_cast<int4*>(w + L.part_list);
     p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);

@@ -73,9 +73,9 @@ constexpr int32_t kMqConsumersNarrow = 2;
 constexpr int32_t kMqConsumersWide = 4;
 
 // A V2 workspace holds two halves of this layout (offsets within a half; `half` is the
-// stride between them).  Consecutive decode calls on one workspace use alternate halves,
-// so that a call's plan kernel may run while the decode kernel of the call before still
-// finishes its last units.
+// size of one): the first at the workspace's start, the second ending at its end.
+// Consecutive decode calls on one workspace use alternate halves, so that a call's plan
+// kernel may run while the decode kernel of the call before still finishes its last units.
 struct WorkspaceLayout {
     size_t hdr, part_list, arrive, part_ml, part_acc, half, total;
 };

@@ -380,3 +380,51 @@ def test_host_argument_errors(cuda_device):
     kc = torch.empty((4, 4, 16, 48), dtype=torch.float16, device=cuda_device)
     with pytest.raises(pa.PAError):
         pa.pa_decode_v1(bad, bad, kc, kc, r.block_tables_d, r.context_lens_d, 9, 0.1)
+
+
+def test_back_to_back_calls_on_one_workspace(cuda_device):
+    """Calls queued back to back on one stream and one workspace, nothing synchronised in
+    between, each with its own queries, lengths and output: the next call's plan / reshape
+    launch while the previous decode finishes its last tiles, on the other half of the
+    workspace.  Every output must still equal the oracle's decode of its own inputs.  Small
+    fixed partitions force many split sequences, and with them partial results and merges
+    in both halves."""
+    pa = _pa()
+    base = W.WORKLOADS["l3_8b"]
+    w = dataclasses.replace(base, num_seqs=48)
+    lens = W.start_context_lens(base)[:48]
+    r = _runner(w, start_lens=lens).next_step()
+    r.run_reshape()
+    _status_ok(r)
+    st = record_step(r)
+    o = OracleState(r, [st])
+    S, Hq, D = w.num_seqs, w.num_q_heads, w.head_size
+    mcl = r.step_max_context_len()
+    ws = torch.empty(max(pa.pa_decode_v2_workspace_size(S, Hq, D, mcl, 64),
+                         pa.pa_decode_auto_workspace_size(S, Hq, w.num_kv_heads, D, w.block_size, mcl)),
+                     dtype=torch.uint8, device=cuda_device)
+    calls = []
+    for k in range(6):
+        # each call attends over a prefix of every context (at least one token) with its
+        # own queries
+        lens_k = np.maximum(r.context_lens - 97 * k, 1).astype(np.int32)
+        q_k = W.randn_16bit((S, Hq, D), w.dtype, 5000 + k, cuda_device)
+        calls.append((lens_k, torch.from_numpy(lens_k).to(cuda_device), q_k, torch.empty_like(q_k)))
+    torch.cuda.synchronize()
+    for k, (lens_k, lens_d, q_k, out_k) in enumerate(calls):
+        if k % 3 == 0:
+            pa.pa_decode_v2(out_k, q_k, r.key_cache, r.value_cache, r.block_tables_d, lens_d, mcl,
+                            w.scale, 64, ws, status=r.status)
+        elif k % 3 == 1:
+            pa.pa_decode_auto(out_k, q_k, r.key_cache, r.value_cache, r.block_tables_d, lens_d,
+                              mcl, w.scale, workspace=ws, status=r.status)
+        else:
+            pa.pa_decode_step(out_k, q_k, r.k_new, r.v_new, r.key_cache, r.value_cache,
+                              r.slots_d, r.block_tables_d, lens_d, mcl, w.scale, workspace=ws,
+                              status=r.status)
+    _status_ok(r)
+    for k, (lens_k, _, q_k, out_k) in enumerate(calls):
+        stq = dataclasses.replace(st, q=bits(q_k))
+        ref = o.decode(0, stq, context_lens=lens_k)
+        e = err_stats(bits(out_k), ref, w.dtype)
+        assert e.ok(w.dtype), f"call {k}: {e}"
