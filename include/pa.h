@@ -143,9 +143,8 @@ size_t pa_decode_v2_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_
  * partition keeps its running max m_p and exp-sum l_p; sequences with more than one
  * partition are merged by log-sum-exp, out = sum_p e^(m_p-M) acc_p / sum_p e^(m_p-M) l_p.
  * `workspace` (device, 256-byte aligned, >= pa_decode_v2_workspace_size bytes) holds the
- * work counter, the partition list and the partial results, twice: consecutive calls on
- * one workspace use its two halves in turn, so that a call's planning may overlap the end
- * of the call before it on the stream.  Its contents need no initialisation. */
+ * work counter, the partition list and the partial results; its contents need no
+ * initialisation and are dead after the call. */
 pa_status pa_decode_v2(void* out, const void* query, const void* key_cache,
                        const void* value_cache, const int32_t* block_tables,
                        int32_t max_blocks_per_seq, const int32_t* context_lens,

@@ -155,18 +155,29 @@ constexpr int kPlanLenCache = 4096;
 // (sequence, kv head) arrival counters.  Entry: (sequence, partition, first partition
 // slot of the sequence, clamped context length).  Partition slots (where partial
 // results go) are numbered sequence by sequence, independent of the claim order.
+//
+// Launched as a programmatic dependent, it may start while the kernel ahead of it on the
+// stream (a decode finishing its last units, a reshape_and_cache) still runs.  Until that
+// kernel has finished it only reads -- the context lengths, which nothing between the two
+// kernels can have rewritten -- and counts; it writes nothing to global memory before
+// grid_dependency_wait(), so that memory the kernel ahead still uses is never touched
+// (a stream-ordered allocator may have handed it out again).
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     __shared__ int32_t scan_buf[32];
     __shared__ int32_t hist[kTailBuckets];    // tail partitions per size bucket
     __shared__ int32_t bstart[kTailBuckets];
     __shared__ unsigned long long total_tokens;
     __shared__ int32_t P_s;
+    __shared__ int32_t bad_len_s;
     __shared__ int32_t len_s[kPlanLenCache];
     allow_dependent_launch();   // the decode kernel may set up meanwhile (it waits for us)
     const int32_t tid = threadIdx.x;
     const int32_t bs = p.block_size;
     for (int32_t i = tid; i < kTailBuckets; i += blockDim.x) hist[i] = 0;
-    if (tid == 0) total_tokens = 0ull;
+    if (tid == 0) {
+        total_tokens = 0ull;
+        bad_len_s = 0;
+    }
     __syncthreads();
     // pass 0: every context length (clamped, errors reported), and the partition size.
     // Fixed (pa_decode_v2), or adaptive: the largest multiple of block_size, not below
@@ -175,11 +186,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     auto len_of = [&](int32_t s) { return cached ? len_s[s] : clamp_len(p, s, false); };
     {
         unsigned long long mine = 0;
+        int32_t bad = 0;
         for (int32_t s = tid; s < p.num_seqs; s += blockDim.x) {
-            const int32_t L = clamp_len(p, s, true);
+            const int32_t L = clamp_len(p, s, false);
+            bad |= L != p.context_lens[s];        // clamped: reported after the wait
             if (cached) len_s[s] = L;
             mine += (unsigned)L;
         }
+        if (bad) bad_len_s = 1;
         if (p.adaptive) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
@@ -224,6 +238,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         full_parts += tf;
     }
     __syncthreads();
+    // Everything below writes global memory: only once the kernel ahead has finished.
+    grid_dependency_wait();
+    if (tid == 0 && bad_len_s && p.status) atomicOr(p.status, kBadLen);
     {   // first list position of each tail bucket: longer tails first
         const int32_t b = kTailBuckets - 1 - tid;
         int32_t tb;
@@ -266,11 +283,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
         p.hdr->partition_size = (uint32_t)P;
         p.hdr->counter = 0;
     }
-    // This kernel may start before the kernel ahead of it on the stream has finished (a
-    // decode running its last units, or a reshape_and_cache): it reads only the context
-    // lengths and writes only this call's half of the workspace.  It finishes only after
-    // that kernel has, so that whatever waits for this one finds everything before done.
-    grid_dependency_wait();
 }
 
 // Moves every sequence to its next token on the device, between the steps of a
@@ -422,9 +434,8 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, voi
 
 cudaError_t launch_plan(const DecodeParams& p, cudaStream_t stream) {
     // Programmatic dependent launch: may start while a preceding reshape_and_cache or
-    // decode kernel still runs.  It rewrites only the half of the workspace that this call
-    // uses, which the decode of the call before on this workspace does not (halves
-    // alternate), and reads only the context lengths, final before the call.
+    // decode kernel still runs; it reads the context lengths meanwhile and writes nothing
+    // before that kernel has finished (see plan_kernel).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
     // one thread per sequence, between kTailBuckets (the bucket scan takes one thread per

@@ -402,19 +402,6 @@ pa_status run_v1(const DecodeArgs& a, const StepReshape* rs = nullptr) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Which half of a V2 workspace the next call on it uses: the halves alternate per
-// workspace, so that two consecutive calls on one stream never share one.
-std::mutex g_half_mu;
-std::unordered_map<const void*, uint32_t> g_half;
-
-uint32_t next_half(const void* ws) {
-    std::lock_guard<std::mutex> lk(g_half_mu);
-    uint32_t& h = g_half[ws];
-    const uint32_t mine = h;
-    h ^= 1u;
-    return mine;
-}
-
 pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_t ws_bytes,
                  bool adaptive = false, const StepReshape* rs = nullptr) {
     DecodeArgs a = a_in;
@@ -444,11 +431,7 @@ pa_status run_v2(const DecodeArgs& a_in, int32_t partition_size, void* ws, size_
     pa::DecodeParams p = base_params(a);
     p.partition_size = partition_size;
     p.adaptive = adaptive ? 1 : 0;
-    // The first half starts at the workspace's start, the second ends at its end: two
-    // consecutive calls with different sizes then never overlap (each call's workspace
-    // holds two of its own halves, so the two halves of any two calls fit side by side).
-    const size_t top = (ws_bytes & ~size_t(255)) - L.half;
-    uint8_t* w = static_cast<uint8_t*>(ws) + (next_half(ws) ? top : 0);
+    uint8_t* w = static_cast<uint8_t*>(ws);
     p.hdr = reinterpret_cast<pa::WsHeader*>(w + L.hdr);
     p.part_list = reinterpret_cast<int4*>(w + L.part_list);
     p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
@@ -538,8 +521,7 @@ WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32
     off = align256(off + sizeof(float2) * (size_t)parts * (size_t)num_q_heads);
     L.part_acc = off;
     off = align256(off + sizeof(float) * (size_t)parts * (size_t)num_q_heads * (size_t)head_size);
-    L.half = off;
-    L.total = 2 * off;
+    L.total = off;
     return L;
 }
 

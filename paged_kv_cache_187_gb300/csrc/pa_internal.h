@@ -72,12 +72,8 @@ constexpr int32_t kMqRowsPerConsumer = 8;
 constexpr int32_t kMqConsumersNarrow = 2;
 constexpr int32_t kMqConsumersWide = 4;
 
-// A V2 workspace holds two halves of this layout (offsets within a half; `half` is the
-// size of one): the first at the workspace's start, the second ending at its end.
-// Consecutive decode calls on one workspace use alternate halves, so that a call's plan
-// kernel may run while the decode kernel of the call before still finishes its last units.
 struct WorkspaceLayout {
-    size_t hdr, part_list, arrive, part_ml, part_acc, half, total;
+    size_t hdr, part_list, arrive, part_ml, part_acc, total;
 };
 
 WorkspaceLayout v2_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,

@@ -48,7 +48,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_device):
     r = _setup()
     mcl = r.step_max_context_len()
     ref64 = OracleState(r, [record_step(r)]).decode(0, record_step(r))
-    for P in (512, 256):
+    for P in (512, 128):
         need = pa.pa_decode_v2_workspace_size(r.w.num_seqs, r.w.num_q_heads, r.w.head_size,
                                               mcl, P)
         assert need <= pa.PA_NOALLOC_SCRATCH_BYTES
