@@ -38,7 +38,12 @@
  *     multiple of num_kv_heads with a group of at most 16; fp16 or bf16.  Other
  *     combinations return PA_ERR_UNSUPPORTED.
  *   Streams.  Every device call is asynchronous on `stream` (a cudaStream_t; NULL is
- *     the legacy default stream) and never synchronises the host.
+ *     the legacy default stream) and never synchronises the host.  The library's kernels
+ *     are launched as programmatic dependents (CUDA programmatic dependent launch): each
+ *     may start before the kernel ahead of it on the stream has finished, and none writes
+ *     global memory before it has waited for that kernel.  A decode kernel lets the kernel
+ *     after it launch once its last tiles are being read; a kernel of the caller's that is
+ *     launched without the programmatic-serialisation attribute is ordered as usual.
  *   Errors.  Calls return a pa_status; pa_last_error() gives this thread's message
  *     for the last failure.  Host-detectable errors (bad sizes, null pointers) are
  *     reported before any launch.  Errors only the device can see (a slot or block-
