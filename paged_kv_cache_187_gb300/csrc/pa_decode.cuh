@@ -80,15 +80,16 @@ __device__ __forceinline__ int32_t clamped_len(const DecodeParams& p, int32_t s,
     return L;
 }
 
-// Named barrier 1 among the consumer warps only (the producer never joins it) that
-// also ORs a flag over every consumer thread, so all consumers take the same branch.
-__device__ __forceinline__ bool consumers_any(bool v, int nthreads) {
+// Named barrier `bar` (1 unless a kernel has several groups of consumer warps) among the
+// consumer warps only (the producer never joins it) that also ORs a flag over every
+// consumer thread, so all consumers take the same branch.
+__device__ __forceinline__ bool consumers_any(bool v, int nthreads, int bar = 1) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "bar.red.or.pred q, %3, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v), "r"(nthreads)
+        : "r"((uint32_t)v), "r"(nthreads), "r"(bar)
         : "memory");
     return r != 0;
 }

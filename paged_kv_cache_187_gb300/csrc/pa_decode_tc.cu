@@ -18,6 +18,13 @@ cudaError_t launch_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const De
     cudaError_t e0 = cudaGetDevice(&dev);
     if (e0 != cudaSuccess) return e0;
     e0 = static_cast<cudaError_t>(configured.run(dev, [&] {
+        // The warpgroups re-divide the registers each thread is launched with (setmaxnreg);
+        // the division is written for REG_LAUNCH per thread and an increase that the
+        // decreases do not cover would wait forever, so any other count is refused here.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != C::REG_LAUNCH) return cudaErrorInvalidKernelImage;
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     }));
     if (e0 != cudaSuccess) return e0;

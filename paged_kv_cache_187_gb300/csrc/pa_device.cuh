@@ -321,6 +321,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Per-thread register budget of the calling warpgroup (PTX "setmaxnreg"): every warp of
+// the warpgroup executes the same call.  A decrease returns registers to the CTA's pool;
+// an increase waits until the pool holds enough, so the increases of a kernel must never
+// exceed what its decreases release from the launch's per-thread count.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_alloc() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_release() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 template <bool kBf16>
 __device__ __forceinline__ uint16_t to16(float x) {
     uint16_t r;

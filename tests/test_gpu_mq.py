@@ -112,6 +112,39 @@ def test_multi_query_decode_matches_oracle(cuda_device, mq_kernel, dtype, QL, Hq
                     assert not bits(out[s, j]).any(), (variant, s, j)
 
 
+@pytest.mark.parametrize("dtype,QL,Hq,Hkv", [("bf16", 4, 32, 8), ("f16", 4, 64, 8)])
+def test_multi_query_runs_of_empty_contexts(cuda_device, mq_kernel, dtype, QL, Hq, Hkv):
+    """Units without a tile (empty contexts) in runs, between and after ordinary ones, on
+    every variant: each such unit still passes its output rows (zero) through the kernel's
+    hand-over in order, so runs of them must neither stall nor disturb their neighbours."""
+    import paged_kv_cache_187_gb300 as pa
+    D, bs = 128, 16
+    lens = [0, 0, 0, 300, 0, 0, 0, 0, 5, 0, 0, 2000, 0, 0, 0, 0, 0, 0, 130, 0, 0, 0]
+    b = _batch(cuda_device, lens, QL, Hq, Hkv, D, bs, dtype, seed=301 + Hq)
+    scale = D ** -0.5
+    ref = oracle.decode_mq(bits(b["q"]), b["okc"], b["ovc"], b["tables"], b["lens"],
+                           np.float32(scale), dtype)
+    S = len(lens)
+    out = torch.empty_like(b["q"])
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    mcl = int(b["lens"].max())
+    ws = torch.empty(max(pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 0),
+                         pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 128), 256),
+                     dtype=torch.uint8, device=cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for variant, psize in (("auto", 0), ("v1", 0), ("v2", 128)):
+        out.fill_(5.0)
+        pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                        variant=variant, partition_size=psize, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, variant
+        assert max_err(bits(out), ref, dtype) <= TOL[dtype], variant
+        for s, L in enumerate(lens):
+            if L == 0:
+                assert not bits(out[s]).any(), (variant, s)
+
+
 def test_multi_query_q_len_one_is_the_ordinary_decode(cuda_device):
     import paged_kv_cache_187_gb300 as pa
     lens = [5, 40, 300, 1000]
