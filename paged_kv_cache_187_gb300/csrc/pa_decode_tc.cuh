@@ -18,7 +18,8 @@
 //   * softmax over the tile's tokens: 4 warps, one tensor-memory lane (token) per thread,
 //     column maxima by a transposed warp reduction plus a cross-warp exchange;
 //   * O^T += V^T P^T:  M = 128 head dims, N = RPAD, K = 128 tokens; A = the V tile
-//     (MN-major), B = P^T (K-major, written by the softmax warps as P_hi + P_lo for bf16);
+//     (MN-major), B = P^T (MN-major: each softmax thread writes its token's row of
+//     weights, as P_hi + P_lo for bf16, in 16-byte stores);
 //     O^T stays in tensor memory and is rescaled there when a row maximum moves.
 // Roles, three warpgroups: warps 0-3 run the softmax; warps 4-7 the epilogue of each unit
 // (O^T out of tensor memory, normalisation, stores, the partition merge), double-buffered
@@ -65,7 +66,12 @@ struct TcCfg {
     static constexpr int NPV = PSPLIT * RPAD_;           // N of the PV product
     static constexpr uint32_t TILE_BYTES = 2 * kHalf;   // K (or V) of one tile: 32 KB
     static constexpr uint32_t QHALF = RPAD_ * 128;      // one 64-dim half of Q
-    static constexpr uint32_t PHALF = NPV * 128;        // one 64-token half of P^T
+    // P^T, the PV's B operand, MN-major: token t's NPV entries (rows n, then the second
+    // term's) fill one PROW-byte row, written by t's softmax thread in 16-byte chunks; the
+    // chunks are swizzled within atoms of 8 rows (128-, 64- or 32-byte swizzle: one MMA's
+    // N entries never cross an atom)
+    static constexpr uint32_t PROW = NPV * 2;           // 128, 64 or 32 bytes per token
+    static constexpr uint32_t PBUF = kTok * PROW;       // one tile's P^T
     // Q buffers (units) and P^T buffers (tiles): two where shared memory allows, so that
     // the next unit's Q, or the next tile's P^T, is written while the MMAs read the
     // current one.  With 32 rows they make room for the rings: one Q buffer (the next
@@ -96,7 +102,7 @@ struct alignas(1024) TcSmem {
     uint8_t k[C::NK][C::TILE_BYTES];
     uint8_t v[C::NV][C::TILE_BYTES];
     uint8_t q[C::NQB][2 * C::QHALF];         // Q of consecutive units
-    uint8_t p[C::NP][2 * C::PHALF];          // P^T of consecutive tiles
+    uint8_t p[C::NP][C::PBUF];               // P^T of consecutive tiles
     alignas(16) float red[2][C::RPAD][4];   // per-warp column maxima, by tile parity
     // A finished unit handed from the softmax to the epilogue warps, by unit parity: the
     // per-warp column exp-sums, the row references and the descriptor
@@ -123,13 +129,6 @@ struct alignas(1024) TcSmem {
 template <class C>
 constexpr size_t tc_smem_bytes() {
     return sizeof(TcSmem<C>) + 1024;
-}
-
-// Byte offset of element (row, col) of a [rows][64] 16-bit block stored as 128-byte rows
-// with the 128B swizzle (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t sw128(int row, int col) {
-    const int byte = col * 2;
-    return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15));
 }
 
 // Lane l ends with the max (sum) over the warp of column l % R of v[0..R).
@@ -432,7 +431,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
                 constexpr uint32_t kIdQK = mma_idesc_f16(C::kBf16, 0, 0, kTok, RPAD);
-                constexpr uint32_t kIdPV = mma_idesc_f16(C::kBf16, 1, 0, kD, C::NPV);
+                constexpr uint32_t kIdPV = mma_idesc_f16(C::kBf16, 1, 1, kD, C::NPV);
                 uint32_t kt = 0, vt = 0, gt = 0, un = 0;
                 bool ok = true;
                 // P^T V of tile t (global tile index), into O^T buffer un & 1.  The first PV of
@@ -448,11 +447,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // descriptors differ from the stage's base only in the start address
                     // (16-byte units, low bits): built once, offset per k-step
                     const uint64_t va = smem_desc_sw128(smem_u32(sm.v[vs]), kHalf, 1024);
-                    const uint64_t pb = smem_desc_sw128(smem_u32(sm.p[t % C::NP]), 16, 1024);
+                    const uint64_t pb = smem_desc(smem_u32(sm.p[t % C::NP]), C::PBUF, 8 * C::PROW, C::PROW);
     #pragma unroll
                     for (int i = 0; i < kTok / 16; ++i)
                         mma_f16_ss(tmem + C::COL_O + (un & 1) * C::NPV, va + (uint64_t)(i * (2048 >> 4)),
-                                   pb + (uint64_t)(((i >> 2) * C::PHALF + (i & 3) * 32) >> 4), kIdPV,
+                                   pb + (uint64_t)((i * 16 * C::PROW) >> 4), kIdPV,
                                    !(first && i == 0));
                     mma_commit(&sm.v_empty[vs]);
                     mma_commit(&sm.pv_done[b]);
@@ -663,19 +662,27 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
                 if (bad) continue;   // the next barrier makes the abort uniform
-                // P^T[n][token] (this thread's token column)
+                // P^T row of this thread's token: the weights rounded to the 16-bit type in
+                // pairs, and for bf16 the rounding remainders as a second term
                 {
-                    const int kh = row >> 6, col = row & 63;
+                    uint32_t w2[C::NPV / 2];
 #pragma unroll
-                    for (int n = 0; n < RPAD; ++n) {
-                        const uint16_t hi = to16<C::kBf16>(x[n]);
-                        *reinterpret_cast<uint16_t*>(pbuf + kh * C::PHALF + sw128(n, col)) = hi;
-                        if constexpr (C::PSPLIT == 2) {
-                            const float hf = __uint_as_float((uint32_t)hi << 16);
-                            *reinterpret_cast<uint16_t*>(pbuf + kh * C::PHALF + sw128(RPAD + n, col)) =
-                                to16<true>(x[n] - hf);
+                    for (int i = 0; i < RPAD / 2; ++i) w2[i] = pack2<C::kBf16>(x[2 * i], x[2 * i + 1]);
+                    if constexpr (C::PSPLIT == 2) {
+#pragma unroll
+                        for (int i = 0; i < RPAD / 2; ++i) {
+                            float h0, h1;
+                            unpack2<true>(w2[i], h0, h1);
+                            w2[RPAD / 2 + i] = pack2<true>(x[2 * i] - h0, x[2 * i + 1] - h1);
                         }
                     }
+                    constexpr int kChunks = C::PROW / 16;
+                    const int swz = (row * (int)C::PROW >> 7) & (kChunks - 1);
+                    uint8_t* const prow = pbuf + row * C::PROW;
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        *reinterpret_cast<uint4*>(prow + ((c ^ swz) << 4)) =
+                            make_uint4(w2[4 * c], w2[4 * c + 1], w2[4 * c + 2], w2[4 * c + 3]);
                 }
                 fence_proxy_async_smem();   // P^T and zeroed V rows -> the tensor core
                 tmem_fence_before_sync();

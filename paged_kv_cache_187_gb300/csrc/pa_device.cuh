@@ -242,11 +242,17 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                  : "memory");
 }
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand: start address, leading
-// and stride byte offsets (16-byte units), descriptor version 1, swizzle mode 128B.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor: start address, leading and stride byte offsets (16-byte
+// units), descriptor version 1, and the swizzle of the operand's rows: 128-, 64- or
+// 32-byte rows whose 16-byte chunks are XOR-swizzled within atoms of 8 rows (descriptor
+// swizzle modes 2, 4 and 6).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t row_bytes) {
+    const uint64_t mode = row_bytes == 128 ? 2 : row_bytes == 64 ? 4 : 6;
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (mode << 61);
+}
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(saddr, lbo, sbo, 128);
 }
 
 // Instruction descriptor of kind::f16 with fp32 accumulation: operand type (fp16 / bf16),
