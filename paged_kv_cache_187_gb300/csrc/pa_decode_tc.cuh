@@ -46,7 +46,7 @@ constexpr int kBarSoft = 1;            // named barrier of the softmax warps
 constexpr int kBarEpi = 2;             // named barrier of the epilogue warps
 // Warp roles (one warpgroup each for the softmax and the epilogue, then the single warps)
 constexpr int kWarpEpi0 = 4, kWarpK = 8, kWarpMma = 9, kWarpV = 10;
-constexpr float kSlack = 8.f;          // weights stay <= 2^kSlack against the reference
+constexpr float kSlack = 8.f;          // a moved reference sits this far above the largest score
 
 template <bool BF16_, int BS_, int RPAD_>
 struct TcCfg {
@@ -85,7 +85,7 @@ struct TcCfg {
     // Registers per thread: the launch gives every thread REG_LAUNCH (65536 / 384, rounded
     // down to a multiple of 8); the epilogue and the single-warp roles hand part of theirs
     // to the softmax warps.  The increase must be covered by the decreases.
-    static constexpr int REG_LAUNCH = 168, REG_SOFT = 224, REG_EPI = 136, REG_AUX = 144;
+    static constexpr int REG_LAUNCH = 168, REG_SOFT = 232, REG_EPI = 128, REG_AUX = 144;
     static_assert(REG_SOFT + REG_EPI + REG_AUX <= 3 * REG_LAUNCH, "register split");
     static_assert(REG_LAUNCH * THREADS <= 65536, "register file");
     // tensor memory: S^T double-buffered (2 x RPAD columns), then O^T of two consecutive
@@ -546,10 +546,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         bool failed = !fetch(0, u);
         // un: units handed to the epilogue warps so far (the current unit's index)
         while (!failed && u.seq >= 0) {
-            // mref[n]: the reference the row's weights are taken against, p = 2^(x - mref).
-            // It only moves when a score exceeds it by more than kSlack (log2 units), so
-            // weights stay <= 2^kSlack and O^T rarely needs rescaling; the result does not
-            // depend on the reference.  ls: this thread's share of the row's weight sum.
+            // mref[n]: the reference of row n's weights, p = 2^(y - mref) for the score y in
+            // log2 units.  When it moves it is set kSlack above the largest score seen, and
+            // it moves only when a score passes it, so weights stay <= 1 and O^T rarely
+            // needs rescaling; the result does not depend on the reference.  -inf: the row
+            // has seen no token yet.  ls: this thread's share of the row's weight sum.
             float mref[RPAD], ls[RPAD];
 #pragma unroll
             for (int n = 0; n < RPAD; ++n) {
@@ -563,6 +564,28 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int32_t tile0 = u.tok0 + j * kTok;
                 const int32_t tok = tile0 + row;
                 const bool ok = !bad && mbar_wait_warp(&sm.s_full[b], (gt >> 1) & 1);
+                // causal limit: query token jq sees tokens below len - q_len + jq + 1, so this
+                // thread's token is seen from query token jmin on, i.e. by the unit's rows
+                // n >= jmin * group - row0 (row n is query token (row0 + n) / group); and
+                // never past the unit's last token
+                const int32_t jmin = max(tok - (u.len - p.q_len), 0);
+                const int32_t nmin = tok < u.tok1 ? jmin * p.group - u.row0 : RPAD;
+                // the tile's scores (S^T column of this thread's token), in log2 units and
+                // masked; S^T stays in tensor memory until this tile's P^T is published
+                auto scores = [&](float (&y)[RPAD]) {
+#pragma unroll
+                    for (int h = 0; h < RPAD / 16; ++h) {
+                        float s16[16];
+                        tmem_ld16(taddr + C::COL_S + b * RPAD + 16 * h, s16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) y[16 * h + i] = s16[i];
+                    }
+#pragma unroll
+                    for (int n = 0; n < RPAD; ++n) y[n] = n >= nmin ? y[n] * p.scale_log2 : -INFINITY;
+                };
+                // x[n]: exponent of the token's weight in row n, y - mref; a positive one
+                // means the reference must move
                 float x[RPAD];
                 bool need = false;
                 if (ok) {
@@ -575,17 +598,21 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) x[16 * h + i] = s16[i];
                     }
-                    // causal limit: query token jq sees tokens below len - q_len + jq + 1, so
-                    // this thread's token is seen from query token jmin on, i.e. by the
-                    // unit's rows n >= jmin * group - row0 (row n is query token
-                    // (row0 + n) / group); and never past the unit's last token
-                    const int32_t jmin = max(tok - (u.len - p.q_len), 0);
-                    const int32_t nmin = tok < u.tok1 ? jmin * p.group - u.row0 : RPAD;
+                    float xmax = -INFINITY;
+                    if (nmin <= 0) {   // every row sees the token
 #pragma unroll
-                    for (int n = 0; n < RPAD; ++n) {
-                        x[n] = n >= nmin ? x[n] * p.scale_log2 : -INFINITY;
-                        need |= x[n] > mref[n] + kSlack;
+                        for (int n = 0; n < RPAD; ++n) {
+                            x[n] = fmaf(x[n], p.scale_log2, -mref[n]);
+                            xmax = fmaxf(xmax, x[n]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int n = 0; n < RPAD; ++n) {
+                            x[n] = n >= nmin ? fmaf(x[n], p.scale_log2, -mref[n]) : -INFINITY;
+                            xmax = fmaxf(xmax, x[n]);
+                        }
                     }
+                    need = xmax > 0.f;
                 }
                 // one barrier per tile: abort together, or move the references together
                 if (consumers_any(!ok || need, kSoftThreads)) {
@@ -593,6 +620,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         failed = true;
                         break;
                     }
+                    scores(x);
                     float cmax[RPAD];
 #pragma unroll
                     for (int n = 0; n < RPAD; ++n) cmax[n] = x[n];
@@ -604,11 +632,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
                     for (int n = 0; n < RPAD; ++n) {
                         const float4 r4 = *reinterpret_cast<const float4*>(sm.red[b][n]);
-                        const float mn = fmaxf(mref[n], fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w)));
+                        const float tmax = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+                        const float mn = tmax > mref[n] ? tmax + kSlack : mref[n];
                         alpha[n] = mref[n] == -INFINITY ? 0.f : fast_exp2(mref[n] - mn);
-                        rescale |= (j > 0 && mref[n] != -INFINITY && mn > mref[n]);
+                        rescale |= (j > 0 && mref[n] != -INFINITY && mn != mref[n]);
                         ls[n] *= alpha[n];
                         mref[n] = mn;
+                        x[n] = mn == -INFINITY ? -INFINITY : x[n] - mn;
                     }
                     if (rescale) {
                         // O^T row (head dim `row`) times alpha per query-row column, once the
@@ -635,8 +665,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
 #pragma unroll
                 for (int n = 0; n < RPAD; ++n) {
-                    // a row that has seen no token yet has no reference: its weights are 0
-                    x[n] = fast_exp2(x[n] - (mref[n] == -INFINITY ? 0.f : mref[n]));
+                    x[n] = fast_exp2(x[n]);   // masked, or no token seen by the row yet: 0
                     ls[n] += x[n];
                 }
                 // P^T buffer gt % NP was last read by the PV of tile gt - NP
