@@ -371,6 +371,28 @@ def run_per_config(args, device, peak):
             fn()
         torch.cuda.synchronize(device)
 
+    def mq_entry(r, QL, desc, record, single_samples):
+        """Multi-query decode (QL causal query tokens per sequence) over r's pools, with its
+        time over the single-query decode kernel's on the same pools."""
+        w = r.w
+        S, Hq, D = w.num_seqs, w.num_q_heads, w.head_size
+        mcl = r.step_max_context_len()
+        q = W.randn_16bit((S, QL, Hq, D), w.dtype, W.stream_seed(w, "q", 1), r.device)
+        o = torch.empty_like(q)
+        wsz = pa.pa_decode_mq_workspace_size(S, QL, Hq, w.num_kv_heads, D, w.block_size, mcl, 0)
+        wsb = torch.empty(max(wsz, 256), dtype=torch.uint8, device=r.device)
+        fn = lambda: pa.pa_decode_mq(o, q, r.key_cache, r.value_cache, r.block_tables_d,
+                                     r.context_lens_d, mcl, w.scale, workspace=wsb, status=r.status)
+        warm(fn)
+        e = _entry(desc, "paged_decode_tc_kernel (tcgen05, auto)",
+                   r.kv_bytes() + 2 * (QL - 1) * S * Hq * D * 2, r.seq_tokens(),
+                   kernel_samples(pa, fn, n, device), peak, record=record,
+                   rows_per_kv_head=QL * Hq // w.num_kv_heads)
+        e["over_single_query_time"] = e["kernel_us"]["mean_us"] / _spread(single_samples)["mean_us"]
+        torch.cuda.synchronize(device)
+        assert int(r.status.item()) == 0
+        return e
+
     # Llama-2-7B MHA, fp16 (CUDA-core path)
     r = runner("l2_7b")
     fn = lambda: r.run_decode("auto")
@@ -413,6 +435,11 @@ def run_per_config(args, device, peak):
     warm(fn)
     ks = kernel_samples(pa, fn, n, device)
     bytes0, tok0 = r.kv_bytes(), r.seq_tokens()
+    # multi-query decode over the same pools, 4 query tokens per sequence: 32 query rows
+    # per kv head (the tcgen05 kernel's 32-row units)
+    out["mq4_l3_70b"] = mq_entry(r, 4, "Llama-3-70B-shaped batch (first step), 4 query tokens "
+                                 "per sequence (causal within them): 32 query rows per kv head",
+                                 "paged_decode_mq4_l3_70b", ks)
     del r, fn
     torch.cuda.empty_cache()
     # the loop starts from the pre-loop lengths: a runner of its own, no step taken yet
@@ -465,24 +492,13 @@ def run_per_config(args, device, peak):
 
     # multi-query decode, 4 query tokens per sequence, over the Llama-3-8B batch's pools
     r = runner("l3_8b")
-    w = r.w
-    QL, S, Hq, D = 4, w.num_seqs, w.num_q_heads, w.head_size
-    mcl = r.step_max_context_len()
-    q = W.randn_16bit((S, QL, Hq, D), w.dtype, W.stream_seed(w, "q", 1), r.device)
-    o = torch.empty_like(q)
-    wsz = pa.pa_decode_mq_workspace_size(S, QL, Hq, w.num_kv_heads, D, w.block_size, mcl, 0)
-    wsb = torch.empty(max(wsz, 256), dtype=torch.uint8, device=r.device)
-    fn = lambda: pa.pa_decode_mq(o, q, r.key_cache, r.value_cache, r.block_tables_d,
-                                 r.context_lens_d, mcl, w.scale, workspace=wsb, status=r.status)
+    fn = lambda: r.run_decode("auto")
     warm(fn)
-    out["mq4_l3_8b"] = _entry("Llama-3-8B-shaped batch, 4 query tokens per sequence (causal "
-                              "within them): 16 query rows per kv head",
-                              "paged_decode_tc_kernel (tcgen05, auto)",
-                              r.kv_bytes() + 2 * (QL - 1) * S * Hq * D * 2, r.seq_tokens(),
-                              kernel_samples(pa, fn, n, device), peak, record="paged_decode_mq4_l3_8b")
-    torch.cuda.synchronize(device)
-    assert int(r.status.item()) == 0
-    del r, q, o, wsb, fn
+    ks = kernel_samples(pa, fn, n, device)
+    out["mq4_l3_8b"] = mq_entry(r, 4, "Llama-3-8B-shaped batch, 4 query tokens per sequence "
+                                "(causal within them): 16 query rows per kv head",
+                                "paged_decode_mq4_l3_8b", ks)
+    del r, fn
     torch.cuda.empty_cache()
     return out
 
