@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from oracle_side import TOL, bits, max_err
+from oracle_side import TOL, bits, err_stats, max_err
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +21,9 @@ def mq_kernel(request, cuda_device):
     pa.pa_set_mq_tcgen05(True)
 
 
-def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
+def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed, k_ramp=None):
+    """Pools for `lens` filled through the product's reshape_and_cache, and their oracle
+    copy.  k_ramp(t, L): optional factor on the K row of token t of a length-L context."""
     import paged_kv_cache_187_gb300 as pa
     from paged_kv_cache_187_gb300 import workloads as W
     lens = np.asarray(lens, np.int32)
@@ -46,6 +48,9 @@ def _batch(dev, lens, QL, Hq, Hkv, D, bs, dtype, seed):
         slots = prod.pa_alloc_slots(s, 0, L)
         assert np.array_equal(slots, ref.slots(s, 0, L))
         k = W.randn_16bit((L, Hkv, D), dtype, seed * 1000 + 2 * s, dev)
+        if k_ramp is not None:
+            f = torch.tensor([k_ramp(t, L) for t in range(L)], dtype=torch.float32, device=dev)
+            k = (k.float() * f[:, None, None]).to(k.dtype)
         v = W.randn_16bit((L, Hkv, D), dtype, seed * 1000 + 2 * s + 1, dev)
         pa.pa_reshape_and_cache(k, v, kc, vc, torch.from_numpy(slots).to(dev), status=status)
         assert oracle.reshape_and_cache(bits(k), bits(v), okc, ovc, slots, bs) == 0
@@ -143,6 +148,44 @@ def test_multi_query_runs_of_empty_contexts(cuda_device, mq_kernel, dtype, QL, H
         for s, L in enumerate(lens):
             if L == 0:
                 assert not bits(out[s]).any(), (variant, s)
+
+
+@pytest.mark.parametrize("dtype,Hq,ramp", [("bf16", 32, "up"), ("bf16", 64, "up"),
+                                           ("f16", 32, "up"), ("bf16", 64, "down")])
+def test_multi_query_moving_references(cuda_device, mq_kernel, dtype, Hq, ramp):
+    """Scores that keep growing along each context (K scaled up token by token, to about
+    13x the first tokens' spread), so that every row's softmax reference moves again in
+    later tiles and the kernels rescale their accumulators in the middle of a unit; and
+    scores that shrink instead (the first tokens dominate, later weights underflow).  16
+    and 32 query rows per kv head, every variant, against the oracle."""
+    import paged_kv_cache_187_gb300 as pa
+    QL, Hkv, D, bs = 4, 8, 128, 16
+    lens = [130, 700, 2100, 4000, 257, 1029]
+    if ramp == "up":
+        k_ramp = lambda t, L: 0.5 + 6.0 * t / L
+    else:
+        k_ramp = lambda t, L: 6.5 - 6.0 * t / L
+    b = _batch(cuda_device, lens, QL, Hq, Hkv, D, bs, dtype, seed=401 + Hq, k_ramp=k_ramp)
+    scale = D ** -0.5
+    ref = oracle.decode_mq(bits(b["q"]), b["okc"], b["ovc"], b["tables"], b["lens"],
+                           np.float32(scale), dtype)
+    S = len(lens)
+    out = torch.empty_like(b["q"])
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    mcl = int(b["lens"].max())
+    ws = torch.empty(max(pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 0),
+                         pa.pa_decode_mq_workspace_size(S, QL, Hq, Hkv, D, bs, mcl, 128), 256),
+                     dtype=torch.uint8, device=cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for variant, psize in (("auto", 0), ("v1", 0), ("v2", 128)):
+        out.fill_(5.0)
+        pa.pa_decode_mq(out, b["q"], b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                        variant=variant, partition_size=psize, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, variant
+        st = err_stats(bits(out), ref, dtype)
+        assert st.ok(dtype), (variant, st)
 
 
 def test_multi_query_q_len_one_is_the_ordinary_decode(cuda_device):
