@@ -188,6 +188,57 @@ def test_multi_query_moving_references(cuda_device, mq_kernel, dtype, Hq, ramp):
         assert st.ok(dtype), (variant, st)
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,bs,ramp", [
+    ("bf16", 32, 8, 128, 16, "up"),    # grouped-query heads: tensor-core path
+    ("f16", 64, 8, 128, 32, "up"),
+    ("bf16", 32, 8, 128, 16, "down"),
+    ("f16", 8, 8, 128, 16, "up"),      # one head per kv head: CUDA-core path
+    ("bf16", 16, 16, 64, 32, "down"),
+])
+def test_single_query_decode_moving_references(cuda_device, dtype, Hq, Hkv, D, bs, ramp):
+    """The ordinary (single-query) decode on contexts whose scores grow, or shrink, along
+    the sequence, so that the running maxima keep moving within a unit and across
+    partitions: V1, V2 with two partition sizes and the automatic choice against the
+    oracle (its multi-query decode with one query token is the ordinary decode)."""
+    import paged_kv_cache_187_gb300 as pa
+    lens = [130, 700, 2100, 4000, 257, 1029]
+    if ramp == "up":
+        k_ramp = lambda t, L: 0.5 + 6.0 * t / L
+    else:
+        k_ramp = lambda t, L: 6.5 - 6.0 * t / L
+    b = _batch(cuda_device, lens, 1, Hq, Hkv, D, bs, dtype, seed=433 + Hq + D, k_ramp=k_ramp)
+    scale = D ** -0.5
+    ref = oracle.decode_mq(bits(b["q"]), b["okc"], b["ovc"], b["tables"], b["lens"],
+                           np.float32(scale), dtype)[:, 0]
+    S = len(lens)
+    q = b["q"][:, 0].contiguous()
+    out = torch.empty_like(q)
+    tables = torch.from_numpy(b["tables"]).to(cuda_device)
+    lens_d = torch.from_numpy(b["lens"]).to(cuda_device)
+    mcl = int(b["lens"].max())
+    ws = torch.empty(max(pa.pa_decode_v2_workspace_size(S, Hq, D, mcl, 2 * bs),
+                         pa.pa_decode_auto_workspace_size(S, Hq, Hkv, D, bs, mcl), 256),
+                     dtype=torch.uint8, device=cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    calls = {
+        "v1": lambda: pa.pa_decode_v1(out, q, b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                                      status=status),
+        "v2_512": lambda: pa.pa_decode_v2(out, q, b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                                          512, ws, status=status),
+        "v2_2bs": lambda: pa.pa_decode_v2(out, q, b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                                          2 * bs, ws, status=status),
+        "auto": lambda: pa.pa_decode_auto(out, q, b["kc"], b["vc"], tables, lens_d, mcl, scale,
+                                          workspace=ws, status=status),
+    }
+    for name, call in calls.items():
+        out.fill_(5.0)
+        call()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, name
+        st = err_stats(bits(out), ref, dtype)
+        assert st.ok(dtype), (name, st)
+
+
 def test_multi_query_q_len_one_is_the_ordinary_decode(cuda_device):
     import paged_kv_cache_187_gb300 as pa
     lens = [5, 40, 300, 1000]
