@@ -16,11 +16,13 @@
 //   * S^T = K Q^T:  M = 128 tokens, N = RPAD (16 or 32) query rows, K = 128 head dims;
 //     A = the K tile (K-major), B = Q (K-major, staged swizzled by the producer);
 //   * softmax over the tile's tokens: 4 warps, one tensor-memory lane (token) per thread,
-//     column maxima by a transposed warp reduction plus a cross-warp exchange;
+//     against a per-row reference that moves only when a score passes it (one vote of
+//     the four warps per tile; column maxima by a transposed warp reduction and a
+//     cross-warp exchange only when it moves);
 //   * O^T += V^T P^T:  M = 128 head dims, N = RPAD, K = 128 tokens; A = the V tile
 //     (MN-major), B = P^T (MN-major: each softmax thread writes its token's row of
 //     weights, as P_hi + P_lo for bf16, in 16-byte stores);
-//     O^T stays in tensor memory and is rescaled there when a row maximum moves.
+//     O^T stays in tensor memory and is rescaled there when a row's reference moves.
 // Roles, three warpgroups: warps 0-3 run the softmax; warps 4-7 the epilogue of each unit
 // (O^T out of tensor memory, normalisation, stores, the partition merge), double-buffered
 // in tensor memory so that the next unit's softmax never waits for it; warp 8 streams K
@@ -59,9 +61,9 @@ struct TcCfg {
     // tile's chain (QK^T, softmax, PV), so K never gets fewer stages than V.
     static constexpr int NK = 3, NV = 3;
     static constexpr int NQ = 2;                  // unit descriptor slots
-    // P as hi + lo bf16 terms, or one fp16 term.  The terms are stacked along N (rows
-    // n and RPAD + n of P^T), so one PV instruction per k-step reads the V tile once and
-    // accumulates O_hi and O_lo side by side; the epilogue adds them.
+    // P as hi + lo bf16 terms, or one fp16 term.  The terms are stacked along N (entries
+    // n and RPAD + n of a token's P^T row), so one PV instruction per k-step reads the V
+    // tile once and accumulates O_hi and O_lo side by side; the epilogue adds them.
     static constexpr int PSPLIT = BF16_ ? 2 : 1;
     static constexpr int NPV = PSPLIT * RPAD_;           // N of the PV product
     static constexpr uint32_t TILE_BYTES = 2 * kHalf;   // K (or V) of one tile: 32 KB
