@@ -196,8 +196,8 @@ struct DecodeArgs {
 // where it measured faster than the mma.sync kernel, whose three CTAs per SM hide the load
 // latency better than its single tile pipeline per SM: above 8 query rows per kv head
 // (Llama-3-8B / -70B batches, decode kernel: 8 rows with 16-token blocks 210 vs 205 us;
-// 16 rows 212 vs 269 us with 16-token blocks, 635 vs 666 us with 32-token blocks; 32 rows
-// 263 vs 395 us and 748 vs 1084 us).
+// 16 rows 203 vs 261 us with 16-token blocks, 617 vs 631 us with 32-token blocks; 32 rows
+// 226 vs 379 us and 667 vs 1061 us).
 #ifndef PA_MQ_TC_ROWS_BS32
 #define PA_MQ_TC_ROWS_BS32 8    // tcgen05 above this many rows per kv head, 32-token blocks
 #endif
