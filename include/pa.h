@@ -251,10 +251,14 @@ pa_status pa_decode_mq(void* out, const void* query, const void* key_cache, cons
 
 /* Selects the multi-query kernel for head_size 128 with 16-bit caches and more than 8
  * query rows (q_len x group) per kv head: 1 (the default) runs it on the 5th-generation
- * tensor cores (tcgen05, accumulators in tensor memory), 0 on mma.sync.  Other shapes, and fixed V2 partition sizes that are not a
- * multiple of 128 tokens, always take the mma.sync kernel.  The setting belongs to the
- * calling thread: it changes that thread's later calls only (each thread starts at 1).
- * Returns PA_OK. */
+ * tensor cores (tcgen05, accumulators in tensor memory), 0 on mma.sync.  Other shapes,
+ * and fixed V2 partition sizes that are not a multiple of 128 tokens, always take the
+ * mma.sync kernel.  The setting belongs to the calling thread: it changes that thread's
+ * later calls only (each thread starts at 1).  Returns PA_OK.
+ * The tcgen05 kernel's warpgroups divide among themselves the registers each thread is
+ * launched with; at its first launch on a device the library checks that the kernel was
+ * compiled with the per-thread count that division assumes, and if not, the call fails
+ * with PA_ERR_CUDA ("invalid kernel image") instead of launching. */
 pa_status pa_set_mq_tcgen05(int32_t enable);
 
 /* One decode step of the hot path on device buffers: pa_reshape_and_cache of the
