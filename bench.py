@@ -371,7 +371,8 @@ def run_per_config(args, device, peak):
             fn()
         torch.cuda.synchronize(device)
 
-    def mq_entry(r, QL, desc, record, single_samples):
+    def mq_entry(r, QL, desc, record, single_samples,
+                 kernel="paged_decode_tc_kernel (tcgen05, auto)"):
         """Multi-query decode (QL causal query tokens per sequence) over r's pools, with its
         time over the single-query decode kernel's on the same pools."""
         w = r.w
@@ -384,7 +385,7 @@ def run_per_config(args, device, peak):
         fn = lambda: pa.pa_decode_mq(o, q, r.key_cache, r.value_cache, r.block_tables_d,
                                      r.context_lens_d, mcl, w.scale, workspace=wsb, status=r.status)
         warm(fn)
-        e = _entry(desc, "paged_decode_tc_kernel (tcgen05, auto)",
+        e = _entry(desc, kernel,
                    r.kv_bytes() + 2 * (QL - 1) * S * Hq * D * 2, r.seq_tokens(),
                    kernel_samples(pa, fn, n, device), peak, record=record,
                    rows_per_kv_head=QL * Hq // w.num_kv_heads)
@@ -498,6 +499,10 @@ def run_per_config(args, device, peak):
     out["mq4_l3_8b"] = mq_entry(r, 4, "Llama-3-8B-shaped batch, 4 query tokens per sequence "
                                 "(causal within them): 16 query rows per kv head",
                                 "paged_decode_mq4_l3_8b", ks)
+    # 2 query tokens: 8 rows per kv head, the mma.sync multi-query kernel
+    out["mq2_l3_8b"] = mq_entry(r, 2, "Llama-3-8B-shaped batch, 2 query tokens per sequence "
+                                "(causal within them): 8 query rows per kv head",
+                                "paged_decode_mq2_l3_8b", ks, kernel="paged_decode_kernel (mma.sync multi-query, auto)")
     del r, fn
     torch.cuda.empty_cache()
     return out

@@ -37,7 +37,7 @@ def test_every_workload_has_a_traffic_record():
     names = {os.path.basename(p)[:-len("_traffic.txt")] for p in RECORDS}
     assert {"paged_decode_l3_8b", "paged_decode_l2_7b", "paged_decode_skew",
             "paged_decode_l3_70b", "paged_decode_fp8_l3_8b", "paged_decode_fp8_l3_70b",
-            "paged_decode_mq4_l3_8b", "paged_decode_mq4_l3_70b"} <= names
+            "paged_decode_mq4_l3_8b", "paged_decode_mq4_l3_70b", "paged_decode_mq2_l3_8b"} <= names
 
 
 def test_traffic_records_match_the_workload_bytes():
